@@ -1,0 +1,137 @@
+"""Seeded synthetic inputs and the named workload shapes.
+
+This module holds no attention arithmetic.  It only draws random numbers and
+describes shapes, so that the CUDA path, the tests, the benchmark and the CPU
+oracle can all be fed the same bytes.
+
+Recipe (stand-in for the RL micro-batches of the DualKV pages, "Experimental
+setup" and "Key results" of the research-map page; their datasets are not used):
+
+* ``torch.Generator('cpu').manual_seed(seed)``; q, k, v, dout drawn in that
+  order with ``torch.randn`` in fp32 (N(0, 1)), then rounded to bf16 (RNE).
+* Ragged response lengths come from ``numpy.random.default_rng(0)``,
+  ``integers(512, 8193, size=16)`` (uniform on [512, 8192]).
+* Packed token order: prompt rows ``[0, P)``, then response 1, ..., response N.
+* Softmax scale ``1/sqrt(d)``.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Sequence
+
+import numpy as np
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One packed micro-batch shape: a shared prompt of ``P`` tokens and
+    ``N = len(R_lens)`` responses.  Heads are ``Hq`` query heads over ``Hkv``
+    key/value heads (grouped-query attention), head size ``d``."""
+
+    name: str
+    Hq: int
+    Hkv: int
+    d: int
+    P: int
+    R_lens: tuple
+
+    @property
+    def N(self) -> int:
+        return len(self.R_lens)
+
+    @property
+    def T(self) -> int:
+        """Packed token count P + sum(R_i)."""
+        return self.P + int(sum(self.R_lens))
+
+    @property
+    def T_replicated(self) -> int:
+        """Token count of the replicated layout sum_i (P + R_i)."""
+        return int(sum(self.P + r for r in self.R_lens))
+
+    @property
+    def offsets(self) -> List[int]:
+        """off_0 = P, off_{i+1} = off_i + R_i; response i is rows [off_i, off_i + R_i)."""
+        out = [self.P]
+        for r in self.R_lens:
+            out.append(out[-1] + int(r))
+        return out
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def pairs_per_head(self) -> int:
+        """Unmasked (query, key) pairs of one head on the packed layout."""
+        P = self.P
+        n = P * (P + 1) // 2
+        for r in self.R_lens:
+            n += r * P + r * (r + 1) // 2
+        return n
+
+    def pairs_per_head_replicated(self) -> int:
+        return sum((self.P + r) * (self.P + r + 1) // 2 for r in self.R_lens)
+
+    def useful_flops(self, fwd: bool = True, bwd: bool = True) -> float:
+        """Useful tensor flops on the packed layout: 4d per pair forward
+        (QK^T and PV), 10d per pair backward (five products)."""
+        per = (4 if fwd else 0) + (10 if bwd else 0)
+        return float(per) * self.d * self.Hq * self.pairs_per_head()
+
+    def rho_tokens(self) -> float:
+        """rho = N(P+R)/(P+NR), the token compression factor."""
+        return self.T_replicated / self.T
+
+    def rho_pairs(self) -> float:
+        return self.pairs_per_head_replicated() / self.pairs_per_head()
+
+    def replicated(self) -> "Workload":
+        """The same micro-batch on the replicated layout: no shared prompt,
+        N independent causal sequences of P + R_i tokens."""
+        return Workload(self.name + "-replicated", self.Hq, self.Hkv, self.d, 0,
+                        tuple(self.P + int(r) for r in self.R_lens))
+
+
+def ragged_lengths(n: int = 16, lo: int = 512, hi: int = 8192, seed: int = 0) -> tuple:
+    return tuple(int(x) for x in np.random.default_rng(seed).integers(lo, hi + 1, size=n))
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 2, 1, 64, 128, (64,) * 4),
+    "qwen3_8b": Workload("qwen3_8b", 32, 8, 128, 4096, (4096,) * 32),
+    "p32k": Workload("p32k", 32, 8, 128, 32768, (2048,) * 16),
+    "ragged_30b_a3b": Workload("ragged_30b_a3b", 32, 4, 128, 8192, ragged_lengths()),
+    "edge_p64k": Workload("edge_p64k", 32, 8, 128, 65536, (1024,) * 16),
+    "edge_n4": Workload("edge_n4", 32, 8, 128, 8192, (8192,) * 4),
+}
+
+
+def make_workload(name: str, Hq: int, Hkv: int, d: int, P: int, R_lens: Sequence[int]) -> Workload:
+    return Workload(name, int(Hq), int(Hkv), int(d), int(P), tuple(int(r) for r in R_lens))
+
+
+@dataclasses.dataclass
+class Inputs:
+    """bf16 CPU tensors in the packed layout: q, dout [T, Hq, d]; k, v [T, Hkv, d]."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    dout: torch.Tensor
+
+
+def make_inputs(w: Workload, seed: int = 0) -> Inputs:
+    g = torch.Generator("cpu").manual_seed(seed)
+    T = w.T
+    q = torch.randn((T, w.Hq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((T, w.Hkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((T, w.Hkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dout = torch.randn((T, w.Hq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return Inputs(q, k, v, dout)
+
+
+def to_f64(x: torch.Tensor) -> np.ndarray:
+    """Exact upcast of a bf16 tensor to a float64 numpy array."""
+    return x.detach().to("cpu").to(torch.float64).numpy()
