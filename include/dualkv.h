@@ -1,0 +1,139 @@
+/*
+ * dualkv.h -- C ABI of the GB300 (sm_103a) exact shared-prompt attention library.
+ *
+ * The operation ("DualKV: Shared-Prompt Flash Attention for Efficient RL
+ * Training with Large Rollouts and Long Contexts"; research-map page, section
+ * "Approach"; arXiv abstract page; forum page, "Two changes"): N response
+ * sequences sampled from one P-token prompt are packed as P + sum_i R_i rows
+ * -- the prompt once, then response 1 .. response N -- instead of N*(P+R)
+ * replicated rows.  Attention on the packed rows is exactly the causal
+ * attention of each replicated sequence [prompt ; response_i]:
+ *   - a prompt row t attends to prompt keys 0..t;
+ *   - a row of response i attends to every prompt key and, causally, to the
+ *     keys of its own response up to and including itself.
+ * The backward pass sums the prompt rows' dK/dV contributions of all N
+ * sequences into the one packed copy.
+ *
+ * Conventions shared by every entry point
+ *   T        = P + sum(R_lens)   packed rows; response i is rows [off_i, off_i + R_i)
+ *            with off_0 = P, off_{i+1} = off_i + R_i.
+ *   q, out, dout, dq : [T, Hq, d]  bf16, row-major, contiguous (device memory)
+ *   k, v, dk, dv     : [T, Hkv, d] bf16, row-major, contiguous (device memory)
+ *   lse              : [Hq, T] fp32 (device) -- natural log of
+ *                      sum_j exp(softmax_scale * q . k_j) over the row's visible keys.
+ *   R_lens           : HOST array of N int32 response lengths, read during the call.
+ *   Grouped-query attention: q-head h reads kv-head h / (Hq / Hkv).
+ *   Accepted shapes: d in {64, 128}; Hq % Hkv == 0; 1 <= N <= 1024; P >= 0;
+ *   R_i >= 0; T < 2^31; every device pointer 16-byte aligned.  T == 0 is a
+ *   no-op.  P == 0 gives N independent causal sequences; N == 1 is one causal
+ *   sequence of P + R_1 rows.  The number of 128-row tiles (ceil(P/128) plus
+ *   sum ceil(R_i/128)) must not exceed 5600 per launch.
+ *   Packed dO of a prompt row is the gradient of the shared prompt row, i.e.
+ *   the sum over the N replicated sequences of that row's gradient.
+ *
+ * Ownership: the caller owns every buffer, the workspace and the stream.  The
+ * library allocates no device memory; the only state it keeps is a per-device
+ * error word and a cached kernel configuration.  All work is enqueued on
+ * `stream` (a cudaStream_t; NULL = legacy default stream) and the calls
+ * return without synchronising.
+ *
+ * Errors: every entry point returns a dualkv_status.  Arguments are checked
+ * before anything is launched; a rejected call launches nothing.  Launch
+ * failures map to DUALKV_ERR_CUDA.  Device-side pipeline waits are bounded;
+ * a wait that gives up records DUALKV_ERR_TIMEOUT in the device error word,
+ * which dualkv_last_device_error() reports.
+ */
+#ifndef DUALKV_H_
+#define DUALKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DUALKV_API __attribute__((visibility("default")))
+#else
+#define DUALKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DUALKV_OK = 0,
+  DUALKV_ERR_INVALID_ARG = 1,  /* null pointer, negative length, N out of range, T mismatch */
+  DUALKV_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, too many tiles */
+  DUALKV_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned */
+  DUALKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
+  DUALKV_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+  DUALKV_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by dualkv_last_device_error) */
+} dualkv_status;
+
+/*
+ * Forward pass (research-map page, "Approach": one fused launch iterating over
+ * the shared-context and per-sequence-response key regions).
+ *   q, k, v       : device inputs, layouts above.
+ *   P, N, R_lens  : packed layout; R_lens is a host array of N entries.
+ *   softmax_scale : multiplies q . k before the softmax (usually 1/sqrt(d)).
+ *   out           : device output [T, Hq, d] bf16 (written for all T rows).
+ *   lse           : device output [Hq, T] fp32, natural-log LSE per row.
+ *   stream        : cudaStream_t to enqueue on.
+ * Returns DUALKV_OK or an error code; on error nothing is launched.
+ */
+DUALKV_API int dualkv_fwd(const void* q, const void* k, const void* v, int64_t P, int32_t N,
+               const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale,
+               void* out, float* lse, void* stream);
+
+/*
+ * Workspace bytes that dualkv_bwd needs for this shape and reduction mode
+ * (0 = fp32 atomics into one prompt accumulator, 1 = deterministic per-split
+ * partials reduced in a fixed order).  num_splits is the number of sequence
+ * chunks a prompt key tile's work is divided into (0 = library choice).
+ * Returns 0 for arguments dualkv_bwd would reject.
+ */
+DUALKV_API size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
+                                  int32_t Hkv, int32_t d, int deterministic, int32_t num_splits);
+
+/*
+ * Backward pass (research-map page, "Approach": fused backward with the shared
+ * prompt's gradients accumulated across the N sequences in fp32).
+ *   q, k, v, out, lse : the forward's inputs and outputs (out and lse exactly
+ *                       as dualkv_fwd wrote them).
+ *   dout              : device [T, Hq, d] bf16 output gradient (prompt rows
+ *                       carry the summed gradient of the shared rows).
+ *   deterministic     : 0 = prompt dK/dV summed with fp32 atomics;
+ *                       1 = per-split fp32 partials summed in a fixed order
+ *                       (bitwise reproducible).
+ *   num_splits        : sequence chunks per prompt key tile (0 = library
+ *                       choice; must match the value given to
+ *                       dualkv_bwd_workspace_bytes).
+ *   workspace         : device scratch of at least dualkv_bwd_workspace_bytes()
+ *                       bytes, 256-byte aligned; contents need not be initialised.
+ *   dq                : device output [T, Hq, d] bf16.
+ *   dk, dv            : device outputs [T, Hkv, d] bf16.
+ * Returns DUALKV_OK or an error code; on error nothing is launched.
+ */
+DUALKV_API int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+               const float* lse, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
+               int32_t Hkv, int32_t d, float softmax_scale, int deterministic, int32_t num_splits,
+               void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream);
+
+/* Static text for a dualkv_status value (never NULL). */
+DUALKV_API const char* dualkv_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns DUALKV_OK, DUALKV_ERR_TIMEOUT (a bounded device wait gave
+ * up; *site, if non-NULL, receives the kernel-specific wait site id) or
+ * DUALKV_ERR_CUDA if the synchronisation itself failed.
+ */
+DUALKV_API int dualkv_last_device_error(void* stream, int32_t* site);
+
+/* Library version as major*10000 + minor*100 + patch. */
+DUALKV_API int dualkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUALKV_H_ */

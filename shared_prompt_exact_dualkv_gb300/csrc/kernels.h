@@ -1,0 +1,40 @@
+// Host-side launchers of the device kernels (one per .cu file).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace dkv {
+
+// Forward: O and LSE for every (query tile, q-head) item of `s`.
+cudaError_t launch_fwd(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK,
+                       const CUtensorMap& mV, void* out, float* lse, unsigned int* err, cudaStream_t stream);
+
+// Backward preprocess: Dvec[h, t] = sum_c dO[t,h,c] * O[t,h,c] (fp32) for all
+// T x Hq rows, and zero `zero_n` floats at `zero_ptr` (the fp32 prompt
+// accumulators of the atomic mode; zero_n may be 0).
+cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, int64_t T, int Hq, int d,
+                              float* zero_ptr, size_t zero_n, cudaStream_t stream);
+
+// dQ: one (query tile, q-head) item per CTA, same key walk as the forward.
+cudaError_t launch_dq(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK,
+                      const CUtensorMap& mV, const CUtensorMap& mdO, const float* lse, const float* Dvec,
+                      void* dq, unsigned int* err, cudaStream_t stream);
+
+// dK/dV: one (key tile, kv-head, split) item per CTA.  Response key rows are
+// written to dk/dv (bf16); prompt key rows go to fp32 `acc_k/acc_v`
+// ([P,Hkv,d]) with atomics when `deterministic` is 0, or to the split's slice
+// of `part_k/part_v` ([S,P,Hkv,d]) when it is 1.
+cudaError_t launch_dkdv(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK,
+                        const CUtensorMap& mV, const CUtensorMap& mdO, const float* lse, const float* Dvec,
+                        void* dk, void* dv, float* acc_k, float* acc_v, int deterministic,
+                        unsigned int* err, cudaStream_t stream);
+
+// Prompt rows of dK/dV: sum the `nsplit` fp32 slices (stride `slice` floats)
+// in split order and round to bf16 (RNE) into dk/dv rows [0, P).
+cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
+                                 void* dk, void* dv, size_t n, cudaStream_t stream);
+
+}  // namespace dkv

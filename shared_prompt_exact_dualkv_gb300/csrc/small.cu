@@ -1,0 +1,114 @@
+// Bandwidth-bound helpers of the backward pass: the D = rowsum(dO * O)
+// preprocess (FlashAttention-2 backward, the lineage named on the DualKV
+// research-map page) and the prompt dK/dV reduction + bf16 cast.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace dkv {
+namespace {
+
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
+  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(pa[i]);
+    const float2 fb = __bfloat1622float2(pb[i]);
+    s = fmaf(fa.x, fb.x, s);
+    s = fmaf(fa.y, fb.y, s);
+  }
+  return s;
+}
+
+// LPR lanes cooperate on one row of d = 8*LPR features.
+template <int LPR>
+__global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                         float* __restrict__ Dvec, int64_t rows, int T, int Hq,
+                                                         float4* __restrict__ zero_ptr, int64_t zero_n4) {
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+  const int sub = threadIdx.x % LPR;
+  // Every lane of a warp stays in the loop while any lane has a row, so the
+  // shuffles below are always warp-convergent.
+  for (int64_t r = tid / LPR; __any_sync(0xffffffffu, r < rows); r += nthreads / LPR) {
+    float s = 0.f;
+    if (r < rows) s = dot8_bf16(__ldg(o + r * LPR + sub), __ldg(dout + r * LPR + sub));
+#pragma unroll
+    for (int m = LPR / 2; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    if (sub == 0 && r < rows) {
+      const int64_t t = r / Hq;
+      const int h = static_cast<int>(r % Hq);
+      Dvec[int64_t(h) * T + t] = s;
+    }
+  }
+  for (int64_t i = tid; i < zero_n4; i += nthreads) zero_ptr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(256) prompt_reduce_kernel(const float4* __restrict__ src_k, const float4* __restrict__ src_v,
+                                                            int nsplit, int64_t slice4, uint2* __restrict__ dk,
+                                                            uint2* __restrict__ dv, int64_t n4) {
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = tid; i < n4; i += nthreads) {
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float4* src = which ? src_v : src_k;
+      float4 a = src[i];
+      for (int sp = 1; sp < nsplit; ++sp) {
+        const float4 b = src[sp * slice4 + i];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      (which ? dv : dk)[i] = pk;
+    }
+  }
+}
+
+int grid_for(int64_t work_threads) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = (work_threads + 255) / 256;
+  const int64_t cap = int64_t(sms) * 8;  // 8 resident 256-thread blocks per SM
+  return static_cast<int>(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, int64_t T, int Hq, int d,
+                              float* zero_ptr, size_t zero_n, cudaStream_t stream) {
+  const int64_t rows = T * Hq;
+  const int lpr = d / 8;
+  const int grid = grid_for(rows * lpr);
+  const int64_t z4 = static_cast<int64_t>(zero_n / 4);
+  if (lpr == 16)
+    preprocess_kernel<16><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
+                                                    Dvec, rows, static_cast<int>(T), Hq,
+                                                    reinterpret_cast<float4*>(zero_ptr), z4);
+  else
+    preprocess_kernel<8><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
+                                                   Dvec, rows, static_cast<int>(T), Hq,
+                                                   reinterpret_cast<float4*>(zero_ptr), z4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice, void* dk,
+                                 void* dv, size_t n, cudaStream_t stream) {
+  const int64_t n4 = static_cast<int64_t>(n / 4);
+  if (n4 == 0) return cudaSuccess;
+  prompt_reduce_kernel<<<grid_for(n4), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(src_k), reinterpret_cast<const float4*>(src_v), nsplit,
+      static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

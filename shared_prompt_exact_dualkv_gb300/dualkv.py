@@ -1,0 +1,160 @@
+"""Python binding of the C ABI in ``include/dualkv.h`` (argument marshalling only).
+
+Every call goes straight to ``libdualkv.so``; all arithmetic runs in the CUDA
+kernels.  There is no fallback: if the library is missing, importing this
+module raises.  PyTorch is used only to own device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdualkv.so")
+
+DUALKV_OK = 0
+DUALKV_ERR_INVALID_ARG = 1
+DUALKV_ERR_UNSUPPORTED = 2
+DUALKV_ERR_ALIGNMENT = 3
+DUALKV_ERR_WORKSPACE = 4
+DUALKV_ERR_CUDA = 5
+DUALKV_ERR_TIMEOUT = 6
+
+EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
+            "dualkv_last_device_error", "dualkv_version")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() "
+                          "(python -m shared_prompt_exact_dualkv_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_i64, c_i32, c_p, c_f = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+    p_i32 = ctypes.POINTER(ctypes.c_int32)
+    lib.dualkv_fwd.argtypes = [c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32, c_i32, c_f, c_p, c_p, c_p]
+    lib.dualkv_fwd.restype = ctypes.c_int
+    lib.dualkv_bwd_workspace_bytes.argtypes = [c_i64, c_i32, p_i32, c_i32, c_i32, c_i32, ctypes.c_int, c_i32]
+    lib.dualkv_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.dualkv_bwd.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32, c_i32, c_f,
+                               ctypes.c_int, c_i32, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p]
+    lib.dualkv_bwd.restype = ctypes.c_int
+    lib.dualkv_status_string.argtypes = [ctypes.c_int]
+    lib.dualkv_status_string.restype = ctypes.c_char_p
+    lib.dualkv_last_device_error.argtypes = [c_p, p_i32]
+    lib.dualkv_last_device_error.restype = ctypes.c_int
+    lib.dualkv_version.argtypes = []
+    lib.dualkv_version.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+class DualKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dualkv_status_string(status)} (status {status})")
+
+
+def dualkv_status_string(status: int) -> str:
+    return lib.dualkv_status_string(int(status)).decode()
+
+
+def _lens(R_lens: Sequence[int]):
+    arr = (ctypes.c_int32 * len(R_lens))(*[int(r) for r in R_lens])
+    return arr
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(st: int, where: str) -> None:
+    if st != DUALKV_OK:
+        raise DualKVError(st, where)
+
+
+def dualkv_fwd(q, k, v, P: int, R_lens: Sequence[int], out, lse, softmax_scale: float,
+               stream=None, check: bool = True) -> int:
+    """Calls dualkv_fwd on device tensors (q/out [T,Hq,d], k/v [T,Hkv,d] bf16, lse [Hq,T] fp32)."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    st = lib.dualkv_fwd(_ptr(q), _ptr(k), _ptr(v), int(P), len(R_lens), _lens(R_lens), Hq, Hkv, d,
+                        float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
+    if check:
+        _check(st, "dualkv_fwd")
+    return st
+
+
+def dualkv_bwd_workspace_bytes(P: int, R_lens: Sequence[int], Hq: int, Hkv: int, d: int,
+                               deterministic: bool, num_splits: int = 0) -> int:
+    return int(lib.dualkv_bwd_workspace_bytes(int(P), len(R_lens), _lens(R_lens), int(Hq), int(Hkv), int(d),
+                                              1 if deterministic else 0, int(num_splits)))
+
+
+def dualkv_bwd(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_scale: float,
+               deterministic: bool, workspace, dq, dk, dv, num_splits: int = 0, stream=None,
+               check: bool = True) -> int:
+    """Calls dualkv_bwd; `workspace` is a uint8 device tensor of at least
+    dualkv_bwd_workspace_bytes(...) bytes."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.dualkv_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P), len(R_lens),
+                        _lens(R_lens), Hq, Hkv, d, float(softmax_scale), 1 if deterministic else 0,
+                        int(num_splits), _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk), _ptr(dv),
+                        _stream(stream))
+    if check:
+        _check(st, "dualkv_bwd")
+    return st
+
+
+def dualkv_last_device_error(stream=None):
+    """Synchronises the stream and returns (status, site) of the device error word."""
+    site = ctypes.c_int32(0)
+    st = lib.dualkv_last_device_error(_stream(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def dualkv_version() -> int:
+    return int(lib.dualkv_version())
+
+
+# --------------------------------------------------------------------------- conveniences
+
+def forward(q, k, v, P: int, R_lens: Sequence[int], softmax_scale: Optional[float] = None, stream=None):
+    """Allocates out/lse and runs dualkv_fwd; returns (out, lse)."""
+    T, Hq, d = q.shape
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    dualkv_fwd(q, k, v, P, R_lens, out, lse, softmax_scale, stream)
+    return out, lse
+
+
+def backward(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_scale: Optional[float] = None,
+             deterministic: bool = False, num_splits: int = 0, stream=None, workspace=None):
+    """Allocates dq/dk/dv (and the workspace unless given) and runs dualkv_bwd."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    if workspace is None:
+        nbytes = dualkv_bwd_workspace_bytes(P, R_lens, Hq, Hkv, d, deterministic, num_splits)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dualkv_bwd(q, k, v, out, dout, lse, P, R_lens, softmax_scale, deterministic, workspace, dq, dk, dv,
+               num_splits=num_splits, stream=stream)
+    return dq, dk, dv
