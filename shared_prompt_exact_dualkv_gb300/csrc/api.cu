@@ -150,11 +150,11 @@ int build_key_sched(Sched* s, const Shape& sh, float scale, int S) {
   std::vector<int> nR(sh.N);
   for (int i = 0; i < sh.N; ++i) nR[i] = ceil_div(sh.R[i], kTile);
   const int nP = ceil_div(sh.P, kTile);
+  // Every (prompt key tile, split) is listed, even one whose sequence chunk
+  // has no query tiles: in deterministic mode it must still write its
+  // (zero) partial slice, which the fixed-order reduce reads.
   for (int j = 0; j < nP; ++j)
-    for (int c = 0; c < S; ++c) {
-      const int64_t cost = prompt_item_cost(sh, j, c, S, nR);
-      if (cost > 0) v.push_back({cost, make_item(j, 0, c)});
-    }
+    for (int c = 0; c < S; ++c) v.push_back({prompt_item_cost(sh, j, c, S, nR), make_item(j, 0, c)});
   for (int i = 0; i < sh.N; ++i)
     for (int j = 0; j < nR[i]; ++j) v.push_back({nR[i] - j, make_item(j, i + 1, 0)});
   return finish_items(s, v);

@@ -1,8 +1,470 @@
+// dK/dV kernel of the backward pass.
+//
+// One CTA owns one 128-row key tile of one kv-head (and, for prompt key
+// tiles, one chunk of the N sequences).  It loops over every query tile that
+// sees those keys, for all q-heads of the kv-head's group (GQA):
+//   * a response key tile of sequence i: the later query tiles of response i
+//     (causal, the first one masked on the diagonal);
+//   * a prompt key tile: the prompt's own later query tiles (split 0 only,
+//     causal) and every query tile of the responses in its chunk (no mask):
+//     the prompt keys are shared by all N sequences (DualKV research-map page,
+//     "Approach"; abstract: the prompt is processed once).
+// Per query tile, with keys on TMEM lanes (FlashAttention-2 style backward):
+//   S^T = K Q^T, P^T = exp(scale*S^T - LSE), dP^T = V dO^T,
+//   dS^T = P^T * (dP^T - D), dV += P^T dO, dK += dS^T Q;  dK *= scale.
+// Response key rows are written as bf16.  Prompt key rows are fp32 partial
+// sums over this CTA's sequences; they are added with fp32 atomics into one
+// accumulator (research-map page, "Approach") or, in deterministic mode,
+// stored per split and summed in a fixed order by the reduce kernel.
+//
+// Warp roles (192 threads): warps 0-3 elementwise (thread r = key row r),
+// warp 4 producer (TMA for Q/dO tiles; its 32 lanes stage the LSE and D
+// vectors of each query tile), warp 5 TMEM allocator + MMA issuer.
+// TMEM columns: S^T [0,128) (P^T bf16 overwrites [0,64) once read),
+// dP^T [128,256) (dS^T bf16 overwrites [128,192)), dV [256,256+D),
+// dK [384,384+D).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
+
 namespace dkv {
-cudaError_t launch_dkdv(const Sched&, int, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                        const CUtensorMap&, const float*, const float*, void*, void*, float*, float*, int,
-                        unsigned int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+template <int D>
+struct DkdvLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;
+  static constexpr int kdO = kQ + kStages * kTileBytes;
+  static constexpr int kVec = kdO + kStages * kTileBytes;  // per stage: lse2[128], D[128] floats
+  static constexpr int kBar = kVec + kStages * 1024;
+  static constexpr int kBytes = kBar + 256 + 1024;
+};
+
+enum DkdvBar {
+  kKVFull = 0,
+  kQFull = 1,    // + stage
+  kQEmpty = 3,   // + stage
+  kSFull = 5,
+  kdPFull = 6,
+  kPReady = 7,
+  kdSReady = 8,
+  kAccDone = 9,
+  kNumDkdvBars = 10
+};
+
+constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
+
+// The query tiles seen by one key-tile item, as "runs" of consecutive tiles
+// of one segment; the walk repeats the runs for each q-head of the group.
+struct QRuns {
+  int32_t seg, j, split, nP, has_prompt, seq_lo, num_runs, per_head, group, hk;
+  int32_t k0, k_end;  // key rows of the item
+
+  __device__ __forceinline__ int32_t seq_tiles(const Sched& s, int i) const {
+    return (s.off[i + 1] - s.off[i] + kTile - 1) / kTile;
+  }
+  __device__ __forceinline__ void init(const Sched& s, uint32_t item, int32_t kvh) {
+    seg = static_cast<int32_t>(item_seg(item));
+    j = static_cast<int32_t>(item_tile(item));
+    split = static_cast<int32_t>(item_split(item));
+    nP = (s.P + kTile - 1) / kTile;
+    group = s.group;
+    hk = kvh;
+    per_head = 0;
+    if (seg == 0) {
+      has_prompt = split == 0 ? 1 : 0;
+      seq_lo = (split * s.N) / s.num_splits;
+      const int seq_hi = ((split + 1) * s.N) / s.num_splits;
+      num_runs = has_prompt + (seq_hi - seq_lo);
+      if (has_prompt) per_head += nP - j;
+      for (int i = seq_lo; i < seq_hi; ++i) per_head += seq_tiles(s, i);
+      k0 = j * kTile;
+      k_end = s.P;
+    } else {
+      has_prompt = 0;
+      seq_lo = seg - 1;
+      num_runs = 1;
+      per_head = seq_tiles(s, seg - 1) - j;
+      k0 = s.off[seg - 1] + j * kTile;
+      k_end = s.off[seg];
+    }
+  }
+};
+
+struct QIter {
+  int32_t hh, r, t;
+  int32_t q_first, t_begin, t_end, seg_end;
+  bool diag_first;
+
+  __device__ __forceinline__ void load_run(const Sched& s, const QRuns& R) {
+    if (R.seg == 0 && R.has_prompt && r == 0) {
+      q_first = 0;
+      t_begin = R.j;
+      t_end = R.nP;
+      seg_end = s.P;
+      diag_first = true;
+    } else {
+      const int i = R.seq_lo + r - R.has_prompt;
+      q_first = s.off[i];
+      t_begin = (R.seg == 0) ? 0 : R.j;
+      t_end = (s.off[i + 1] - s.off[i] + kTile - 1) / kTile;
+      seg_end = s.off[i + 1];
+      diag_first = R.seg != 0;
+    }
+    t = t_begin;
+  }
+  __device__ __forceinline__ void skip_empty(const Sched& s, const QRuns& R) {
+    while (t >= t_end) {
+      if (++r == R.num_runs) {
+        r = 0;
+        ++hh;
+      }
+      load_run(s, R);
+    }
+  }
+  // Position on the first query tile (the item must have per_head > 0).
+  __device__ __forceinline__ void start(const Sched& s, const QRuns& R) {
+    hh = 0;
+    r = 0;
+    load_run(s, R);
+    skip_empty(s, R);
+  }
+  __device__ __forceinline__ void next(const Sched& s, const QRuns& R) {
+    ++t;
+    skip_empty(s, R);
+  }
+  __device__ __forceinline__ int32_t q0() const { return q_first + t * kTile; }
+  __device__ __forceinline__ bool diag() const { return diag_first && t == t_begin; }
+  __device__ __forceinline__ int32_t head(const QRuns& R) const { return R.hk * R.group + hh; }
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    dkdv_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
+                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
+                const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                float* __restrict__ acc_k, float* __restrict__ acc_v, int deterministic, unsigned int* err) {
+  using L = DkdvLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 128);
+  float* vec = reinterpret_cast<float*>(sm + L::kVec);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t item = s.items[blockIdx.x / s.Hkv];
+  const int hk = blockIdx.x % s.Hkv;
+  QRuns R;
+  R.init(s, item, hk);
+  const int n = R.per_head * R.group;
+
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 128) {
+    mbar_init(&bar[kKVFull], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[kQFull + i], 1);
+      mbar_init(&bar[kQEmpty + i], 1);
+    }
+    mbar_init(&bar[kSFull], 1);
+    mbar_init(&bar[kdPFull], 1);
+    mbar_init(&bar[kPReady], 128);
+    mbar_init(&bar[kdSReady], 128);
+    mbar_init(&bar[kAccDone], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (n > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar[kKVFull], 2 * L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(sm + L::kK + a * 16384, &mK, &bar[kKVFull], a * 64, hk, R.k0);
+          tma_load_3d(sm + L::kV + a * 16384, &mV, &bar[kKVFull], a * 64, hk, R.k0);
+        }
+      }
+      QIter it;
+      it.start(s, R);
+      for (int i = 0; i < n; ++i, (i < n ? it.next(s, R) : void())) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&bar[kQEmpty + st], ((i >> 1) - 1) & 1, err, 701)) break;
+        const int h = it.head(R);
+        const int q0 = it.q0();
+        float* vl = vec + st * 256;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cidx = lane * 4 + u;
+          const int q = q0 + cidx;
+          float l2 = INFINITY, dd = 0.f;
+          if (q < it.seg_end) {
+            l2 = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
+            dd = Dvec[static_cast<size_t>(h) * s.T + q];
+          }
+          vl[cidx] = l2;
+          vl[128 + cidx] = dd;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[kQFull + st], 2 * L::kTileBytes);
+          for (int a = 0; a < D / 64; ++a) {
+            tma_load_3d(sm + L::kQ + st * L::kTileBytes + a * 16384, &mQ, &bar[kQFull + st], a * 64, h, q0);
+            tma_load_3d(sm + L::kdO + st * L::kTileBytes + a * 16384, &mdO, &bar[kQFull + st], a * 64, h, q0);
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idG = idesc_bf16(128, D, false, true);
+      const uint32_t sK = smem_u32(sm + L::kK);
+      const uint32_t sV = smem_u32(sm + L::kV);
+      bool ok = mbar_wait(&bar[kKVFull], 0, err, 801);
+      auto issue_s = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(&bar[kQFull + st], (i >> 1) & 1, err, 802)) return false;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + L::kQ + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + kColS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(sQ + off), idSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[kSFull]);
+        return true;
+      };
+      auto issue_dp = [&](int i) {
+        const int st = i & 1;
+        const uint32_t sdO = smem_u32(sm + L::kdO + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + kColdP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sdO + off), idSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[kdPFull]);
+      };
+      if (ok) {
+        ok = issue_s(0);
+        if (ok) issue_dp(0);
+      }
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i & 1;
+        // dV += P^T dO  (P^T read from TMEM columns [0,64))
+        if (!mbar_wait(&bar[kPReady], i & 1, err, 803)) break;
+        tc_fence_after();
+        const uint32_t sdO = smem_u32(sm + L::kdO + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + kColdV, tmem + kColS + kk * 8, desc_mnmajor_sw128(sdO + kk * 2048, 16384), idG,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        // the next S^T may overwrite P^T: it is issued after the dV product
+        if (i + 1 < n && !issue_s(i + 1)) break;
+        // dK += dS^T Q  (dS^T read from TMEM columns [128,192))
+        if (!mbar_wait(&bar[kdSReady], i & 1, err, 804)) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + L::kQ + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + kColdK, tmem + kColdP + kk * 8, desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar[kQEmpty + st]);
+        if (i + 1 < n) issue_dp(i + 1);
+      }
+      mma_commit(&bar[kAccDone]);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int row = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = s.scale_log2;
+    bool ok = n > 0;
+    if (ok) {
+      QIter it;
+      it.start(s, R);
+      for (int i = 0; i < n; ++i, (i < n ? it.next(s, R) : void())) {
+        const int st = i & 1;
+        const float* vl = vec + st * 256;
+        if (!mbar_wait(&bar[kQFull + st], (i >> 1) & 1, err, 901)) { ok = false; break; }
+        if (!mbar_wait(&bar[kSFull], i & 1, err, 902)) { ok = false; break; }
+        tc_fence_after();
+        float p[128];
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + kColS + ci * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) p[ci * 32 + u] = __uint_as_float(r[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 128; u += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(vl + u);
+          p[u] = ex2(fmaf(p[u], c, -l4.x));
+          p[u + 1] = ex2(fmaf(p[u + 1], c, -l4.y));
+          p[u + 2] = ex2(fmaf(p[u + 2], c, -l4.z));
+          p[u + 3] = ex2(fmaf(p[u + 3], c, -l4.w));
+        }
+        if (it.diag()) {
+#pragma unroll
+          for (int u = 0; u < 128; ++u) p[u] = (u < row) ? 0.f : p[u];
+        }
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) pk[u] = pack_bf16x2(p[ci * 32 + 2 * u], p[ci * 32 + 2 * u + 1]);
+          tmem_st16(tmem + lane_off + kColS + ci * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[kPReady]);
+
+        if (!mbar_wait(&bar[kdPFull], i & 1, err, 903)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + kColdP + ci * 32, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int cc = ci * 32 + 2 * u;
+            const float2 d2 = *reinterpret_cast<const float2*>(vl + 128 + cc);
+            const float a0 = p[cc] * (__uint_as_float(r[2 * u]) - d2.x);
+            const float a1 = p[cc + 1] * (__uint_as_float(r[2 * u + 1]) - d2.y);
+            pk[u] = pack_bf16x2(a0, a1);
+          }
+          tmem_st16(tmem + lane_off + kColdP + ci * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[kdSReady]);
+      }
+    }
+    // ---------------------------------------------------------------- epilogue
+    const int k = R.k0 + row;
+    const bool valid = k < R.k_end;
+    const bool prompt_item = R.seg == 0;
+    if (ok) ok = mbar_wait(&bar[kAccDone], 0, err, 904);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) tc_fence_after();
+    if (prompt_item) {
+      // fp32 partial of this CTA's sequences for prompt key row k
+      const size_t base = (static_cast<size_t>(k) * s.Hkv + hk) * D;
+      const size_t slice = static_cast<size_t>(s.P) * s.Hkv * D;
+      float* pk_out = acc_k + (deterministic ? R.split * slice : 0) + base;
+      float* pv_out = acc_v + (deterministic ? R.split * slice : 0) + base;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which ? kColdK : kColdV;
+        const float mul = which ? s.scale : 1.f;
+        float* dst = which ? pk_out : pv_out;
+#pragma unroll
+        for (int ci = 0; ci < D / 32; ++ci) {
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld32(tmem + lane_off + col + ci * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) r[u] = 0u;
+          }
+          if (valid && (ok || n == 0)) {
+#pragma unroll
+            for (int u = 0; u < 32; u += 4) {
+              const float a0 = __uint_as_float(r[u]) * mul, a1 = __uint_as_float(r[u + 1]) * mul;
+              const float a2 = __uint_as_float(r[u + 2]) * mul, a3 = __uint_as_float(r[u + 3]) * mul;
+              if (deterministic)
+                *reinterpret_cast<float4*>(dst + ci * 32 + u) = make_float4(a0, a1, a2, a3);
+              else if (n > 0)
+                red_add_v4(dst + ci * 32 + u, a0, a1, a2, a3);
+            }
+          }
+        }
+      }
+    } else if (ok) {
+      const size_t base = (static_cast<size_t>(k) * s.Hkv + hk) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which ? kColdK : kColdV;
+        const float mul = which ? s.scale : 1.f;
+        uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + base);
+#pragma unroll
+        for (int ci = 0; ci < D / 32; ++ci) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + col + ci * 32, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const Sched& s, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                          const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dk, void* dv,
+                          float* acc_k, float* acc_v, int deterministic, unsigned int* err, cudaStream_t stream) {
+  using L = DkdvLayout<D>;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hkv);
+  dkdv_kernel<D><<<grid, 192, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
+                                                   static_cast<__nv_bfloat16*>(dv), acc_k, acc_v, deterministic, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dkdv(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                        const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dk, void* dv,
+                        float* acc_k, float* acc_v, int deterministic, unsigned int* err, cudaStream_t stream) {
+  if (s.num_items == 0) return cudaSuccess;
+  return d == 64 ? launch_dkdv_d<64>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, deterministic, err, stream)
+                 : launch_dkdv_d<128>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, deterministic, err,
+                                      stream);
+}
+
 }  // namespace dkv

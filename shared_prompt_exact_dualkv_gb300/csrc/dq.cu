@@ -1,7 +1,305 @@
+// dQ kernel of the backward pass.
+//
+// One CTA owns one 128-row query tile of one q-head and walks the same two
+// key regions as the forward (shared prompt, then the query's own response;
+// DualKV research-map page, "Approach").  Per key tile it recomputes the
+// probabilities from the saved LSE (FlashAttention-2 style backward, the
+// lineage named on the research-map page):
+//   S = Q K^T, P = exp(scale*S - LSE), dP = dO V^T, dS = P * (dP - D),
+//   dQ += dS K,   and finally dQ *= scale.
+// A CTA is the only writer of its dQ rows, so dQ needs no atomics.
+//
+// Warp roles (192 threads): warps 0-3 elementwise (thread r = query row r),
+// warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+// TMEM columns: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16, two per
+// column) double buffer [384,448) and [448,512).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
+
 namespace dkv {
-cudaError_t launch_dq(const Sched&, int, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                      const CUtensorMap&, const float*, const float*, void*, unsigned int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+template <int D>
+struct DqLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kQ = 0;
+  static constexpr int kdO = kQ + kTileBytes;
+  static constexpr int kK = kdO + kTileBytes;
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kBar = kV + kVStages * kTileBytes;
+  static constexpr int kBytes = kBar + 256 + 1024;
+};
+
+enum DqBar {
+  kQFull = 0,
+  kKFull = 1,    // + stage (3)
+  kKEmpty = 4,   // + stage (3)
+  kVFull = 7,    // + stage (2)
+  kVEmpty = 9,   // + stage (2)
+  kSFull = 11,
+  kSFree = 12,
+  kdPFull = 13,
+  kdPFree = 14,
+  kdSFull = 15,  // + buffer (2)
+  kdSFree = 17,  // + buffer (2)
+  kNumDqBars = 19
+};
+
+constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 256, kColdS = 384;
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    dq_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
+              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+              const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
+              const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, unsigned int* err) {
+  using L = DqLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 192);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t item = s.items[blockIdx.x / s.Hq];
+  const int h = blockIdx.x % s.Hq;
+  const int hk = h / s.group;
+  KeyWalk w;
+  w.init(s, item);
+  const int n = w.n;
+
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 128) {
+    mbar_init(&bar[kQFull], 1);
+    for (int i = 0; i < L::kKStages; ++i) {
+      mbar_init(&bar[kKFull + i], 1);
+      mbar_init(&bar[kKEmpty + i], 1);
+    }
+    for (int i = 0; i < L::kVStages; ++i) {
+      mbar_init(&bar[kVFull + i], 1);
+      mbar_init(&bar[kVEmpty + i], 1);
+    }
+    mbar_init(&bar[kSFull], 1);
+    mbar_init(&bar[kSFree], 128);
+    mbar_init(&bar[kdPFull], 1);
+    mbar_init(&bar[kdPFree], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[kdSFull + i], 128);
+      mbar_init(&bar[kdSFree + i], 1);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar[kQFull], 2 * L::kTileBytes);
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
+        tma_load_3d(sm + L::kdO + a * 16384, &mdO, &bar[kQFull], a * 64, h, w.q0);
+      }
+      int ks = 0, kph = 0, vs = 0, vph = 0;
+      for (int j = 0; j < n; ++j) {
+        const int k0 = w.k0(j);
+        if (j >= L::kKStages && !mbar_wait(&bar[kKEmpty + ks], kph ^ 1, err, 401)) break;
+        mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sm + L::kK + ks * L::kTileBytes + a * 16384, &mK, &bar[kKFull + ks], a * 64, hk, k0);
+        if (j >= L::kVStages && !mbar_wait(&bar[kVEmpty + vs], vph ^ 1, err, 402)) break;
+        mbar_arrive_expect_tx(&bar[kVFull + vs], L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sm + L::kV + vs * L::kTileBytes + a * 16384, &mV, &bar[kVFull + vs], a * 64, hk, k0);
+        if (++ks == L::kKStages) { ks = 0; kph ^= 1; }
+        if (++vs == L::kVStages) { vs = 0; vph ^= 1; }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idQ = idesc_bf16(128, D, false, true);
+      const uint32_t sQ = smem_u32(sm + L::kQ);
+      const uint32_t sdO = smem_u32(sm + L::kdO);
+      bool ok = mbar_wait(&bar[kQFull], 0, err, 501);
+      // S_j = Q K_j^T and dP_j = dO V_j^T
+      auto issue_s = [&](int j) -> bool {
+        const int ks = j % L::kKStages;
+        if (!mbar_wait(&bar[kKFull + ks], (j / L::kKStages) & 1, err, 502)) return false;
+        if (j >= 1 && !mbar_wait(&bar[kSFree], (j - 1) & 1, err, 503)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + kColS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[kSFull]);
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {
+        const int vs = j % L::kVStages;
+        if (!mbar_wait(&bar[kVFull + vs], (j / L::kVStages) & 1, err, 504)) return false;
+        if (j >= 1 && !mbar_wait(&bar[kdPFree], (j - 1) & 1, err, 505)) return false;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + kColdP, desc_kmajor_sw128(sdO + off), desc_kmajor_sw128(sV + off), idSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[kdPFull]);
+        mma_commit(&bar[kVEmpty + vs]);
+        return true;
+      };
+      if (ok) ok = issue_s(0) && issue_dp(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !(issue_s(j + 1) && issue_dp(j + 1))) break;
+        const int b = j & 1;
+        if (!mbar_wait(&bar[kdSFull + b], (j >> 1) & 1, err, 506)) break;
+        tc_fence_after();
+        const int ks = j % L::kKStages;
+        const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          mma_ts(tmem + kColdQ, tmem + kColdS + b * 64 + kk * 8, desc_mnmajor_sw128(sK + kk * 2048, 16384), idQ,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar[kdSFree + b]);
+        mma_commit(&bar[kKEmpty + ks]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int row = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = s.scale_log2;
+    const int q = w.q0 + row;
+    // Rows past the segment end are never stored; give them P = 0.
+    float lse2 = INFINITY, Dr = 0.f;
+    if (q < w.q_end) {
+      lse2 = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
+      Dr = Dvec[static_cast<size_t>(h) * s.T + q];
+    }
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&bar[kSFull], j & 1, err, 601)) { ok = false; break; }
+      tc_fence_after();
+      float p[128];
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColS + ci * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[ci * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[kSFree]);
+#pragma unroll
+      for (int i = 0; i < 128; ++i) p[i] = ex2(fmaf(p[i], c, -lse2));
+      const int mk = w.mask_kind(j);
+      if (mk == 1) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) p[i] = (i > row) ? 0.f : p[i];
+      } else if (mk == 2) {
+        const int lim = w.P - w.k0(j);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) p[i] = (i >= lim) ? 0.f : p[i];
+      }
+      if (!mbar_wait(&bar[kdPFull], j & 1, err, 602)) { ok = false; break; }
+      tc_fence_after();
+      // dS buffer b was last read by the dQ product of tile j-2.
+      if (j >= 2 && !mbar_wait(&bar[kdSFree + b], ((j >> 1) - 1) & 1, err, 603)) { ok = false; break; }
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColdP + ci * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = p[ci * 32 + 2 * i] * (__uint_as_float(r[2 * i]) - Dr);
+          const float d1 = p[ci * 32 + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - Dr);
+          pk[i] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tmem + lane_off + kColdS + b * 64 + ci * 16, pk);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[kdPFree]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[kdSFull + b]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    const int bl = (n - 1) & 1;
+    if (ok) ok = n > 0 && mbar_wait(&bar[kdSFree + bl], ((n - 1) >> 1) & 1, err, 604);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const bool valid = q < w.q_end;
+      uint4* dst = reinterpret_cast<uint4*>(dq + (static_cast<size_t>(q) * s.Hq + h) * D);
+#pragma unroll
+      for (int ci = 0; ci < D / 32; ++ci) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColdQ + ci * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * s.scale, __uint_as_float(r[2 * i + 1]) * s.scale);
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
+
+template <int D>
+cudaError_t launch_dq_d(const Sched& s, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                        const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, unsigned int* err,
+                        cudaStream_t stream) {
+  using L = DqLayout<D>;
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hq);
+  dq_kernel<D><<<grid, 192, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dq), err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dq(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                      const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, unsigned int* err,
+                      cudaStream_t stream) {
+  if (s.num_items == 0) return cudaSuccess;
+  return d == 64 ? launch_dq_d<64>(s, mQ, mK, mV, mdO, lse, Dvec, dq, err, stream)
+                 : launch_dq_d<128>(s, mQ, mK, mV, mdO, lse, Dvec, dq, err, stream);
+}
+
 }  // namespace dkv

@@ -38,12 +38,13 @@ enum FwdBar {
   kQFull = 0,
   kKFull = 1,     // + stage
   kVFull = 3,     // + stage
-  kKVEmpty = 5,   // + stage
-  kSFull = 7,     // + buffer
-  kSFree = 9,     // + buffer
-  kPFull = 11,
-  kODone = 12,
-  kNumFwdBars = 13
+  kKEmpty = 5,    // + stage: released once QK^T has read it
+  kVEmpty = 7,    // + stage: released once PV has read it
+  kSFull = 9,     // + buffer
+  kSFree = 11,    // + buffer
+  kPFull = 13,
+  kODone = 14,
+  kNumFwdBars = 15
 };
 
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384;
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kKFull + i], 1);
       mbar_init(&bar[kVFull + i], 1);
-      mbar_init(&bar[kKVEmpty + i], 1);
+      mbar_init(&bar[kKEmpty + i], 1);
+      mbar_init(&bar[kVEmpty + i], 1);
       mbar_init(&bar[kSFull + i], 1);
       mbar_init(&bar[kSFree + i], 128);
     }
@@ -100,12 +102,13 @@ __global__ void __launch_bounds__(192, 1)
       for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&bar[kKVEmpty + st], ((j >> 1) - 1) & 1, err, 101)) break;
         const int k0 = w.k0(j);
         uint8_t* sK = sm + L::kK + st * L::kTileBytes;
         uint8_t* sV = sm + L::kV + st * L::kTileBytes;
+        if (j >= 2 && !mbar_wait(&bar[kKEmpty + st], ((j >> 1) - 1) & 1, err, 101)) break;
         mbar_arrive_expect_tx(&bar[kKFull + st], L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + st], a * 64, hk, k0);
+        if (j >= 2 && !mbar_wait(&bar[kVEmpty + st], ((j >> 1) - 1) & 1, err, 102)) break;
         mbar_arrive_expect_tx(&bar[kVFull + st], L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
       }
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(192, 1)
           mma_ss(dS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar[kSFull + st]);
+        mma_commit(&bar[kKEmpty + st]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(192, 1)
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bar[kODone]);
-        mma_commit(&bar[kKVEmpty + st]);
+        mma_commit(&bar[kVEmpty + st]);
       }
     }
   } else {
@@ -237,7 +241,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&bar[kPFull]);
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok && mbar_wait(&bar[kODone], (n - 1) & 1, err, 303)) {
+    if (ok) ok = mbar_wait(&bar[kODone], (n - 1) & 1, err, 303);
+    if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int q = w.q0 + row;
       const bool valid = q < w.q_end;

@@ -89,7 +89,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 #define DKV_WAIT_LIMIT_NS 1000000000ull
 #endif
 
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned int* err,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned int* err,
                                             uint32_t site, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
