@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the exact shared-prompt attention layer (forward + backward).
+
+A step is one forward and one backward of one attention layer on the packed
+P + N*R layout (all rows of the hot path: forward, D preprocess, dK/dV with
+the prompt reduction, dQ), with inputs resident in HBM.  Default workload:
+32 query / 8 KV heads, d = 128, P = 32768, N = 16, R = 2048 (packed 65,536
+rows), bf16 N(0,1) inputs from the seeded generator.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own
+independent replica of the layer (weak scaling, no data-path collective); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from shared_prompt_exact_dualkv_gb300 import synthetic  # noqa: E402
+
+METRIC = "DualKV fwd+bwd ms and useful TFLOP/s (% of GB300 bf16 peak) per attn layer"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != self.gpu_index:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of `x` over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job useful TFLOP/s: the units all ranks processed over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
+# --------------------------------------------------------------------------- CPU oracle timings
+
+def _oracle_seq0_inputs(w: synthetic.Workload, seed: int):
+    L = w.P + w.R_lens[0]
+    g = torch.Generator("cpu").manual_seed(seed)
+    return [torch.randn((L, 1, w.d), generator=g).to(torch.bfloat16).to(torch.float64).numpy() for _ in range(4)]
+
+
+def oracle_sample_seconds(w: synthetic.Workload, seed: int = 0):
+    """The fp64 oracle (as it stands) on one q-head and sequence 0 of the
+    workload: replicated fwd + bwd of [prompt ; response_0]."""
+    from oracle import attention as ora
+    q, k, v, do = _oracle_seq0_inputs(w, seed)
+    t0 = time.perf_counter()
+    ora.dualkv_forward(q, k, v, w.P, (w.R_lens[0],), w.scale)
+    ora.dualkv_backward(q, k, v, do, w.P, (w.R_lens[0],), w.scale)
+    dt = time.perf_counter() - t0
+    sub = synthetic.make_workload("s", 1, 1, w.d, w.P, (w.R_lens[0],))
+    return dt, sub.useful_flops()
+
+
+def oracle_rows_seconds(w: synthetic.Workload, rows: int, seed: int = 0):
+    """The oracle's row-wise function on `rows` query rows of q-head 0 in
+    sequence 0 (O, LSE and dQ of each row over its full visible key set).
+    Credited work: 8*d flops per visible (query, key) pair (QK^T, PV, dO V^T,
+    dS K)."""
+    from oracle import attention as ora
+    rng = np.random.default_rng(seed)
+    q, k, v, do = _oracle_seq0_inputs(w, seed)
+    L = q.shape[0]
+    picks = np.sort(rng.choice(L, size=min(rows, L), replace=False))
+    t0 = time.perf_counter()
+    ora.rows_forward_backward(q, k, v, do, w.P, (w.R_lens[0],), w.scale, [0], picks.tolist())
+    dt = time.perf_counter() - t0
+    pairs = int(sum(int(t) + 1 for t in picks))
+    return dt, 8.0 * w.d * pairs
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores (rank 0 only), on the same workload."""
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    # per-step sample sized so that warm-up + timed steps stay within ~2.5 minutes
+    probe_dt, _ = oracle_rows_seconds(w, 16, seed=99)
+    per_row = probe_dt / 16
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = int(max(8, min(4096, budget / max(per_row, 1e-6))))
+    for i in range(args.warmup):
+        oracle_rows_seconds(w, rows, seed=i)
+    tot_t, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_rows_seconds(w, rows, seed=1000 + i)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "P": w.P, "N": w.N,
+                   "R": list(w.R_lens[:1]) if len(set(w.R_lens)) == 1 else list(w.R_lens)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"per step: O, LSE and dQ of {rows} random query rows of q-head 0 in "
+                                   f"sequence 0 (fp64 row-wise oracle), credited 8*d flops per visible pair"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="p32k", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--deterministic", action="store_true", help="time the deterministic dK/dV mode")
+    ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from shared_prompt_exact_dualkv_gb300 import dualkv as D
+
+    w = synthetic.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = synthetic.make_inputs(w, seed=rank)
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.dout))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    det = bool(args.deterministic)
+    ws = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, det), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        D.dualkv_fwd(q, k, v, w.P, w.R_lens, out, lse, w.scale, stream)
+        D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, det, ws, dq, dk, dv, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / args.steps
+    st, site = D.dualkv_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error {st} at wait site {site}")
+
+    # per-kernel device time (events around each launch, same stream)
+    D.dualkv_trace_enable(True)
+    for _ in range(args.steps):
+        step()
+    tr = D.dualkv_trace_read()
+    D.dualkv_trace_enable(False)
+    per_kernel = {name: (tot / cnt if cnt else 0.0) for name, (tot, cnt) in tr.items()}
+    launches_per_step = sum(cnt for _, cnt in tr.values()) // args.steps
+
+    # end to end: pinned host buffers in, results out, through the same C ABI calls
+    hin = [t.pin_memory() for t in (x.q, x.k, x.v, x.dout)]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for dst, src in zip((q, k, v, do), hin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hout, (out, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+
+    flops = w.useful_flops()
+    value = weak_scaling_value(flops, ms, world)
+    e2e_value = weak_scaling_value(flops, e2e_ms, world)
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+
+    # dominant kernel: dK/dV (four products per unmasked pair: S^T, dP^T, dV, dK)
+    dkdv_ms = per_kernel.get("bwd_dkdv", 0.0)
+    dkdv_flops = 8.0 * w.d * w.Hq * w.pairs_per_head()
+    dkdv_tf = dkdv_flops / (dkdv_ms * 1e-3) / 1e12 if dkdv_ms else None
+    roofline = {"bound": "tensor", "kernel": "dkdv_kernel", "achieved": dkdv_tf, "peak": peak_sus,
+                "unit": "TFLOP/s", "frac": (dkdv_tf / peak_sus) if dkdv_tf else None, "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "algorithmic": "8*d flops per unmasked (query,key) pair per q-head"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "P": w.P, "N": w.N,
+                   "R": list(w.R_lens[:1]) if len(set(w.R_lens)) == 1 else list(w.R_lens),
+                   "T_packed": w.T, "T_replicated": w.T_replicated, "rho_tokens": round(w.rho_tokens(), 3),
+                   "rho_pairs": round(w.rho_pairs(), 3), "useful_tflop_per_step": flops / 1e12,
+                   "dkdv_mode": "deterministic" if det else "atomic",
+                   "l2": "inputs larger than L2 (q alone %.0f MB > 129 MB)" % (q.numel() * 2 / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": value / world / peak_sus,
+        "per_kernel_ms": per_kernel,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": roofline,
+    }
+
+    if rank == 0 and not args.quick:
+        # the other reduction mode of the prompt dK/dV
+        ws2 = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, not det), dtype=torch.uint8,
+                          device=dev)
+        for _ in range(2):
+            D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, not det, ws2, dq, dk, dv, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, not det, ws2, dq, dk, dv, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        result["bwd_ms_other_mode"] = {"mode": "atomic" if det else "deterministic", "ms": a.elapsed_time(b) / 3}
+        del ws2
+        # the same library on the replicated N(P+R) layout
+        wr = w.replicated()
+        gen = torch.Generator(device=dev).manual_seed(7)
+        rq = torch.randn((wr.T, w.Hq, w.d), device=dev, generator=gen).to(torch.bfloat16)
+        rk = torch.randn((wr.T, w.Hkv, w.d), device=dev, generator=gen).to(torch.bfloat16)
+        rv = torch.randn((wr.T, w.Hkv, w.d), device=dev, generator=gen).to(torch.bfloat16)
+        rdo = torch.randn((wr.T, w.Hq, w.d), device=dev, generator=gen).to(torch.bfloat16)
+        rout, rlse = torch.empty_like(rq), torch.empty((w.Hq, wr.T), dtype=torch.float32, device=dev)
+        rdq, rdk, rdv = torch.empty_like(rq), torch.empty_like(rk), torch.empty_like(rv)
+        rws = torch.empty(max(1, D.dualkv_bwd_workspace_bytes(0, wr.R_lens, w.Hq, w.Hkv, w.d, False)),
+                          dtype=torch.uint8, device=dev)
+
+        def rstep():
+            D.dualkv_fwd(rq, rk, rv, 0, wr.R_lens, rout, rlse, w.scale, stream)
+            D.dualkv_bwd(rq, rk, rv, rout, rdo, rlse, 0, wr.R_lens, w.scale, False, rws, rdq, rdk, rdv, stream=stream)
+
+        rstep()
+        a.record(stream)
+        for _ in range(2):
+            rstep()
+        b.record(stream)
+        torch.cuda.synchronize()
+        rms = a.elapsed_time(b) / 2
+        result["replicated_layout"] = {"ms_per_step": rms, "T": wr.T, "speedup_packed": rms / ms,
+                                       "useful_tflop_replicated": wr.useful_flops() / 1e12}
+        del rq, rk, rv, rdo, rout, rlse, rdq, rdk, rdv, rws
+        torch.cuda.empty_cache()
+        if world == 1:
+            dt, fl = oracle_sample_seconds(w)
+            result["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                "seconds": dt,
+                "sample": f"fp64 oracle fwd+bwd of q-head 0 on sequence 0 ([prompt; response_0], "
+                          f"{w.P + w.R_lens[0]} rows); BLAS multithreaded, elementwise single-threaded"}
+        st, site = D.dualkv_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error {st} at wait site {site}")
+
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -129,6 +129,22 @@ DUALKV_API const char* dualkv_status_string(int status);
  */
 DUALKV_API int dualkv_last_device_error(void* stream, int32_t* site);
 
+/*
+ * Launch tracing (profiling aid).  dualkv_trace_enable(1) makes every later
+ * dualkv_fwd / dualkv_bwd call in this process bracket each kernel it
+ * launches with a pair of CUDA events recorded on the call's stream;
+ * dualkv_trace_enable(0) stops that.  Enabling also clears the accumulated
+ * totals.  dualkv_trace_read() synchronises on the recorded events and
+ * returns, per kernel id, the summed device milliseconds and the launch
+ * count since the last enable:
+ *   0 forward, 1 backward preprocess (D = rowsum(dO*O)), 2 dK/dV,
+ *   3 prompt dK/dV reduce + cast, 4 dQ.
+ * `n` is the length of both arrays (at most 5 entries are written).
+ * Events come from a pool owned by the library; no device memory is used.
+ */
+DUALKV_API int dualkv_trace_enable(int on);
+DUALKV_API int dualkv_trace_read(double* ms, int64_t* launches, int32_t n);
+
 /* Library version as major*10000 + minor*100 + patch. */
 DUALKV_API int dualkv_version(void);
 

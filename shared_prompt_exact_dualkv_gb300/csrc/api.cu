@@ -188,6 +188,60 @@ WsLayout workspace_layout(const Shape& sh, int deterministic, int S) {
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : DUALKV_ERR_CUDA; }
 
+// ------------------------------------------------------------------ tracing
+constexpr int kTraceKernels = 5;
+
+struct Trace {
+  std::mutex mu;
+  bool on = false;
+  struct Rec {
+    int kernel;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  double ms[kTraceKernels] = {};
+  int64_t launches[kTraceKernels] = {};
+
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+};
+
+Trace& trace() {
+  static Trace t;
+  return t;
+}
+
+// Brackets one launch with events when tracing is on.
+struct TraceScope {
+  int kernel;
+  cudaStream_t stream;
+  cudaEvent_t a = nullptr, b = nullptr;
+  TraceScope(int k, cudaStream_t s) : kernel(k), stream(s) {
+    Trace& t = trace();
+    std::lock_guard<std::mutex> lock(t.mu);
+    if (!t.on) return;
+    a = t.get();
+    b = t.get();
+    if (a) cudaEventRecord(a, stream);
+  }
+  ~TraceScope() {
+    if (!a || !b) return;
+    cudaEventRecord(b, stream);
+    Trace& t = trace();
+    std::lock_guard<std::mutex> lock(t.mu);
+    t.pending.push_back({kernel, a, b});
+  }
+};
+
 }  // namespace
 }  // namespace dkv
 
@@ -229,6 +283,7 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int64_t P, int32_t N
     return DUALKV_ERR_CUDA;
   unsigned int* err = error_word_ptr();
   if (!err) return DUALKV_ERR_CUDA;
+  TraceScope ts(0, static_cast<cudaStream_t>(stream));
   return map_cuda(launch_fwd(*s, d, mQ, mK, mV, out, lse, err, static_cast<cudaStream_t>(stream)));
 }
 
@@ -276,14 +331,64 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
   float* acc_k = reinterpret_cast<float*>(wb + ws.acc_k);
   float* acc_v = reinterpret_cast<float*>(wb + ws.acc_v);
 
-  cudaError_t e = launch_preprocess(out, dout, Dvec, sh.T, Hq, d, det ? nullptr : acc_k,
-                                    det ? 0 : 2 * (ws.acc_v - ws.acc_k) / 4, cs);
-  if (e == cudaSuccess)
+  cudaError_t e;
+  {
+    TraceScope ts(1, cs);
+    e = launch_preprocess(out, dout, Dvec, sh.T, Hq, d, det ? nullptr : acc_k,
+                          det ? 0 : 2 * (ws.acc_v - ws.acc_k) / 4, cs);
+  }
+  if (e == cudaSuccess) {
+    TraceScope ts(2, cs);
     e = launch_dkdv(*sk, d, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, det, err, cs);
-  if (e == cudaSuccess && sh.P > 0)
+  }
+  if (e == cudaSuccess && sh.P > 0) {
+    TraceScope ts(3, cs);
     e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, ws.slice, cs);
-  if (e == cudaSuccess) e = launch_dq(*sq, d, mQ, mK, mV, mdO, lse, Dvec, dq, err, cs);
+  }
+  if (e == cudaSuccess) {
+    TraceScope ts(4, cs);
+    e = launch_dq(*sq, d, mQ, mK, mV, mdO, lse, Dvec, dq, err, cs);
+  }
   return map_cuda(e);
+}
+
+int dualkv_trace_enable(int on) {
+  Trace& t = trace();
+  std::lock_guard<std::mutex> lock(t.mu);
+  for (auto& r : t.pending) {
+    cudaEventSynchronize(r.b);
+    t.pool.push_back(r.a);
+    t.pool.push_back(r.b);
+  }
+  t.pending.clear();
+  for (int i = 0; i < kTraceKernels; ++i) {
+    t.ms[i] = 0.0;
+    t.launches[i] = 0;
+  }
+  t.on = on != 0;
+  return DUALKV_OK;
+}
+
+int dualkv_trace_read(double* ms, int64_t* launches, int32_t n) {
+  if ((!ms && !launches) || n < 0) return DUALKV_ERR_INVALID_ARG;
+  Trace& t = trace();
+  std::lock_guard<std::mutex> lock(t.mu);
+  int status = DUALKV_OK;
+  for (auto& r : t.pending) {
+    float el = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&el, r.a, r.b) != cudaSuccess)
+      status = DUALKV_ERR_CUDA;
+    t.ms[r.kernel] += el;
+    t.launches[r.kernel] += 1;
+    t.pool.push_back(r.a);
+    t.pool.push_back(r.b);
+  }
+  t.pending.clear();
+  for (int i = 0; i < n && i < kTraceKernels; ++i) {
+    if (ms) ms[i] = t.ms[i];
+    if (launches) launches[i] = t.launches[i];
+  }
+  return status;
 }
 
 int dualkv_last_device_error(void* stream, int32_t* site) {

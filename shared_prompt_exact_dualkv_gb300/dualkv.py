@@ -24,7 +24,9 @@ DUALKV_ERR_CUDA = 5
 DUALKV_ERR_TIMEOUT = 6
 
 EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
-            "dualkv_last_device_error", "dualkv_version")
+            "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version")
+
+TRACE_KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_prompt_reduce", "bwd_dq")
 
 
 def _load() -> ctypes.CDLL:
@@ -45,6 +47,10 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_status_string.restype = ctypes.c_char_p
     lib.dualkv_last_device_error.argtypes = [c_p, p_i32]
     lib.dualkv_last_device_error.restype = ctypes.c_int
+    lib.dualkv_trace_enable.argtypes = [ctypes.c_int]
+    lib.dualkv_trace_enable.restype = ctypes.c_int
+    lib.dualkv_trace_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), c_i32]
+    lib.dualkv_trace_read.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -123,6 +129,19 @@ def dualkv_last_device_error(stream=None):
     site = ctypes.c_int32(0)
     st = lib.dualkv_last_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def dualkv_trace_enable(on: bool) -> None:
+    _check(lib.dualkv_trace_enable(1 if on else 0), "dualkv_trace_enable")
+
+
+def dualkv_trace_read() -> dict:
+    """{kernel name: (total device ms, launches)} since the last enable."""
+    n = len(TRACE_KERNELS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(lib.dualkv_trace_read(ms, cnt, n), "dualkv_trace_read")
+    return {name: (ms[i], cnt[i]) for i, name in enumerate(TRACE_KERNELS)}
 
 
 def dualkv_version() -> int:
