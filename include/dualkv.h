@@ -118,6 +118,38 @@ DUALKV_API int dualkv_bwd(const void* q, const void* k, const void* v, const voi
                int32_t Hkv, int32_t d, float softmax_scale, int deterministic, int32_t num_splits,
                void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream);
 
+/*
+ * Backward pass without any allocation (the DualKV pages have no counterpart;
+ * this entry point exists for callers of this library, not for the method).
+ * Some callers cannot call cudaMalloc or ask an allocator for memory at the
+ * moment they run the backward pass: code running under a memory manager
+ * that owns every byte of the device, code that must not synchronise (which
+ * cudaMalloc/cudaFree can do), or plain-C hosts with no allocator at hand.
+ * This variant takes the same arguments as dualkv_bwd minus the workspace
+ * and uses instead a fixed scratch buffer of DUALKV_STATIC_SCRATCH_BYTES
+ * (16 MiB) that lives inside the library as a device-global array; every
+ * GPU that loads the library keeps those 16 MiB until the process exits.
+ * The caller still owns and passes every input and output.
+ *   - Shapes whose dualkv_bwd_workspace_bytes() exceeds 16 MiB are rejected
+ *     with DUALKV_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the buffer's device address
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls share the one buffer and it keeps the last call's contents;
+ *     the backward pass initialises every part of it that it reads, so no
+ *     clearing is needed between calls.  Two calls whose kernels can run at
+ *     the same time on the GPU (e.g. on unordered streams) race on the
+ *     buffer and give wrong results: order them on one stream or with events.
+ *   - It calls no cudaMalloc, cudaFree or allocating routine.
+ * Returns the same status codes as dualkv_bwd.
+ */
+#define DUALKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+DUALKV_API int dualkv_bwd_static_workspace(const void* q, const void* k, const void* v, const void* out,
+                                           const void* dout, const float* lse, int64_t P, int32_t N,
+                                           const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                           float softmax_scale, int deterministic, int32_t num_splits, void* dq,
+                                           void* dk, void* dv, void* stream);
+
 /* Static text for a dualkv_status value (never NULL). */
 DUALKV_API const char* dualkv_status_string(int status);
 

@@ -403,4 +403,44 @@ int dualkv_last_device_error(void* stream, int32_t* site) {
   return static_cast<int>(w & 0xFFu) == DUALKV_ERR_TIMEOUT ? DUALKV_ERR_TIMEOUT : DUALKV_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ fixed scratch
+// Backward pass for callers that cannot allocate: the workspace is this
+// file-scope device array instead of caller memory.  In host code the name
+// g_static_scratch is only a host-side stand-in for the symbol; its device
+// address comes from cudaGetSymbolAddress, looked up once per device with
+// that device current and cached.
+static __device__ __align__(256) unsigned char g_static_scratch[DUALKV_STATIC_SCRATCH_BYTES];
+
+static void* static_scratch_device_ptr() {
+  static void* cache[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+    cache[dev] = ptr;
+  }
+  return cache[dev];
+}
+
+int dualkv_bwd_static_workspace(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                const float* lse, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
+                                int32_t Hkv, int32_t d, float softmax_scale, int deterministic, int32_t num_splits,
+                                void* dq, void* dk, void* dv, void* stream) {
+  Shape sh;
+  const int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
+  if (st != DUALKV_OK) return st;
+  if (sh.T == 0)
+    return dualkv_bwd(q, k, v, out, dout, lse, P, N, R_lens, Hq, Hkv, d, softmax_scale, deterministic, num_splits,
+                      nullptr, 0, dq, dk, dv, stream);
+  const size_t need = dualkv_bwd_workspace_bytes(P, N, R_lens, Hq, Hkv, d, deterministic, num_splits);
+  if (need > DUALKV_STATIC_SCRATCH_BYTES) return DUALKV_ERR_WORKSPACE;
+  void* ws = static_scratch_device_ptr();
+  if (!ws) return DUALKV_ERR_CUDA;
+  return dualkv_bwd(q, k, v, out, dout, lse, P, N, R_lens, Hq, Hkv, d, softmax_scale, deterministic, num_splits,
+                    ws, DUALKV_STATIC_SCRATCH_BYTES, dq, dk, dv, stream);
+}
+
 }  // extern "C"

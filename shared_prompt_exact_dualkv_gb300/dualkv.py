@@ -24,7 +24,11 @@ DUALKV_ERR_CUDA = 5
 DUALKV_ERR_TIMEOUT = 6
 
 EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
-            "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version")
+            "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
+            "dualkv_bwd_static_workspace")
+
+# Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 16 << 20
 
 TRACE_KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_prompt_reduce", "bwd_dq")
 
@@ -51,6 +55,9 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_trace_enable.restype = ctypes.c_int
     lib.dualkv_trace_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), c_i32]
     lib.dualkv_trace_read.restype = ctypes.c_int
+    lib.dualkv_bwd_static_workspace.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32,
+                                                 c_i32, c_f, ctypes.c_int, c_i32, c_p, c_p, c_p, c_p]
+    lib.dualkv_bwd_static_workspace.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -121,6 +128,24 @@ def dualkv_bwd(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_s
                         _stream(stream))
     if check:
         _check(st, "dualkv_bwd")
+    return st
+
+
+def dualkv_bwd_static_workspace(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_scale: float,
+                                deterministic: bool, dq, dk, dv, num_splits: int = 0, stream=None,
+                                check: bool = True) -> int:
+    """Backward pass that allocates nothing: the library's own fixed 16 MiB
+    device scratch replaces the workspace (for callers that cannot allocate
+    device memory when they run the backward pass).  Calls that can overlap on
+    the GPU share that scratch and must be ordered by the caller."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    st = lib.dualkv_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P),
+                                         len(R_lens), _lens(R_lens), Hq, Hkv, d, float(softmax_scale),
+                                         1 if deterministic else 0, int(num_splits), _ptr(dq), _ptr(dk), _ptr(dv),
+                                         _stream(stream))
+    if check:
+        _check(st, "dualkv_bwd_static_workspace")
     return st
 
 
