@@ -1,0 +1,122 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol that
+include/dualkv.h declares, and rejects bad arguments with the documented
+status codes before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dualkv.h")
+
+
+@pytest.fixture(scope="module")
+def D():
+    from shared_prompt_exact_dualkv_gb300 import build
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+    from shared_prompt_exact_dualkv_gb300 import dualkv
+    return dualkv
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"DUALKV_API\s+[\w\s\*]+?\b(dualkv_\w+)\s*\(", text)
+
+
+def test_header_declares_expected_entry_points():
+    names = set(declared_functions())
+    assert {"dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
+            "dualkv_last_device_error"} <= names
+
+
+def test_library_exports_every_declared_symbol(D):
+    for name in declared_functions():
+        assert hasattr(D.lib, name), name
+    assert set(declared_functions()) == set(D.EXPORTED)
+
+
+def test_status_strings(D):
+    for code in range(0, 8):
+        assert isinstance(D.dualkv_status_string(code), str) and D.dualkv_status_string(code)
+    assert D.dualkv_version() >= 100
+
+
+def _lens(*r):
+    return (ctypes.c_int32 * len(r))(*r)
+
+
+A = 1 << 20  # a 16-byte aligned fake device address; never dereferenced on these paths
+
+
+def fwd(D, **kw):
+    args = dict(q=A, k=A, v=A, P=128, N=2, R=_lens(64, 64), Hq=2, Hkv=1, d=64, scale=0.125, out=A, lse=A)
+    args.update(kw)
+    return D.lib.dualkv_fwd(args["q"], args["k"], args["v"], args["P"], args["N"], args["R"], args["Hq"],
+                            args["Hkv"], args["d"], args["scale"], args["out"], args["lse"], None)
+
+
+def bwd(D, **kw):
+    args = dict(q=A, k=A, v=A, out=A, dout=A, lse=A, P=128, N=2, R=_lens(64, 64), Hq=2, Hkv=1, d=64,
+                scale=0.125, det=0, splits=0, ws=A, ws_bytes=1 << 30, dq=A, dk=A, dv=A)
+    args.update(kw)
+    return D.lib.dualkv_bwd(args["q"], args["k"], args["v"], args["out"], args["dout"], args["lse"], args["P"],
+                            args["N"], args["R"], args["Hq"], args["Hkv"], args["d"], args["scale"], args["det"],
+                            args["splits"], args["ws"], args["ws_bytes"], args["dq"], args["dk"], args["dv"], None)
+
+
+def test_fwd_argument_errors(D):
+    assert fwd(D, N=0) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, N=1025) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, R=None) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, P=-1) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, R=_lens(64, -1)) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, d=96) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd(D, Hq=3, Hkv=2) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd(D, Hkv=0) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, q=None) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, lse=None) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(D, k=A + 8) == D.DUALKV_ERR_ALIGNMENT
+    assert fwd(D, out=A + 2) == D.DUALKV_ERR_ALIGNMENT
+    assert fwd(D, scale=float("nan")) == D.DUALKV_ERR_INVALID_ARG
+    # more 128-row tiles than one launch schedules
+    assert fwd(D, P=0, N=1, R=_lens(128 * 6000)) == D.DUALKV_ERR_UNSUPPORTED
+    # empty input is a no-op, whatever the pointers
+    assert fwd(D, P=0, N=2, R=_lens(0, 0), q=None, out=None) == D.DUALKV_OK
+
+
+def test_bwd_argument_errors(D):
+    assert bwd(D, N=0) == D.DUALKV_ERR_INVALID_ARG
+    assert bwd(D, d=32) == D.DUALKV_ERR_UNSUPPORTED
+    assert bwd(D, dout=None) == D.DUALKV_ERR_INVALID_ARG
+    assert bwd(D, dq=A + 4) == D.DUALKV_ERR_ALIGNMENT
+    assert bwd(D, ws=None) == D.DUALKV_ERR_WORKSPACE
+    assert bwd(D, ws_bytes=16) == D.DUALKV_ERR_WORKSPACE
+    assert bwd(D, ws=A + 16) == D.DUALKV_ERR_ALIGNMENT
+    assert bwd(D, P=0, N=1, R=_lens(0)) == D.DUALKV_OK
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("P,R,Hq,Hkv,d", [(128, (64, 64, 64, 64), 2, 1, 64), (300, (200, 0, 131), 4, 2, 128),
+                                          (0, (77,), 2, 2, 128)])
+def test_workspace_bytes(D, P, R, Hq, Hkv, d):
+    T = P + sum(R)
+    slice_ = P * Hkv * d * 4
+    atomic = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, False, 0)
+    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    for S in (1, 2, 3):
+        det = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, True, S)
+        S_eff = max(1, min(S, len(R)))
+        assert det == _align256(T * Hq * 4) + 2 * _align256(S_eff * slice_)
+    assert D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, 96, False, 0) == 0
+
+
+def test_trace_api_on_cpu(D):
+    D.dualkv_trace_enable(True)
+    assert all(v == (0.0, 0) for v in D.dualkv_trace_read().values())
+    D.dualkv_trace_enable(False)
+    assert D.lib.dualkv_trace_read(None, None, 5) == D.DUALKV_ERR_INVALID_ARG
