@@ -17,12 +17,15 @@
 // accumulator (research-map page, "Approach") or, in deterministic mode,
 // stored per split and summed in a fixed order by the reduce kernel.
 //
-// Warp roles (192 threads): warps 0-3 elementwise (thread r = key row r),
-// warp 4 producer (TMA for Q/dO tiles; its 32 lanes stage the LSE and D
-// vectors of each query tile), warp 5 TMEM allocator + MMA issuer.
-// TMEM columns: S^T [0,128) (P^T bf16 overwrites [0,64) once read),
-// dP^T [128,256) (dS^T bf16 overwrites [128,192)), dV [256,256+D),
-// dK [384,384+D).
+// Warp roles (320 threads): warps 0-7 elementwise -- warp w handles key rows
+// 32*(w%4) .. +31 (its TMEM lane quarter) and query columns 64*(w/4) .. +63,
+// so each row is split over two warps and every SM sub-partition runs two
+// elementwise warps; warp 8 producer (TMA for Q/dO tiles; its 32 lanes stage
+// the LSE and D vectors of each query tile); warp 9 TMEM allocator + MMA issuer.
+// TMEM columns: S^T [0,128); dP^T [128,256); dV [256,256+D); dK [384,384+D).
+// Each half writes its bf16 P^T over the S^T columns it has already read
+// (query half h -> columns [64h, 64h+32)), and likewise dS^T over dP^T, so
+// the two halves never touch each other's unread columns.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -58,6 +61,11 @@ enum DkdvBar {
 };
 
 constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
+constexpr int kEwThreads = 256;  // elementwise threads (two per key row)
+
+// TMEM column offset of the K=16 slice kk of a bf16 operand stored as two
+// 32-column halves at +0 and +64 (queries 0..63 and 64..127).
+__device__ __forceinline__ uint32_t split_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 // The query tiles seen by one key-tile item, as "runs" of consecutive tiles
 // of one segment; the walk repeats the runs for each q-head of the group.
@@ -149,7 +157,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     dkdv_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
@@ -170,11 +178,11 @@ __global__ void __launch_bounds__(192, 1)
   R.init(s, item, hk);
   const int n = R.per_head * R.group;
 
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 256) {
     mbar_init(&bar[kKVFull], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kQFull + i], 1);
@@ -182,8 +190,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(&bar[kSFull], 1);
     mbar_init(&bar[kdPFull], 1);
-    mbar_init(&bar[kPReady], 128);
-    mbar_init(&bar[kdSReady], 128);
+    mbar_init(&bar[kPReady], kEwThreads);
+    mbar_init(&bar[kdSReady], kEwThreads);
     mbar_init(&bar[kAccDone], 1);
     fence_mbar_init();
     tma_prefetch_desc(&mQ);
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (n > 0) {
       if (lane == 0) {
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
@@ -274,23 +282,23 @@ __global__ void __launch_bounds__(192, 1)
       }
       for (int i = 0; ok && i < n; ++i) {
         const int st = i & 1;
-        // dV += P^T dO  (P^T read from TMEM columns [0,64))
+        // dV += P^T dO  (P^T read from TMEM columns [0,32) and [64,96))
         if (!mbar_wait(&bar[kPReady], i & 1, err, 803)) break;
         tc_fence_after();
         const uint32_t sdO = smem_u32(sm + L::kdO + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + kColdV, tmem + kColS + kk * 8, desc_mnmajor_sw128(sdO + kk * 2048, 16384), idG,
+          mma_ts(tmem + kColdV, tmem + kColS + split_col(kk), desc_mnmajor_sw128(sdO + kk * 2048, 16384), idG,
                  (i > 0 || kk > 0) ? 1u : 0u);
         // the next S^T may overwrite P^T: it is issued after the dV product
         if (i + 1 < n && !issue_s(i + 1)) break;
-        // dK += dS^T Q  (dS^T read from TMEM columns [128,192))
+        // dK += dS^T Q  (dS^T read from TMEM columns [128,160) and [192,224))
         if (!mbar_wait(&bar[kdSReady], i & 1, err, 804)) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(sm + L::kQ + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + kColdK, tmem + kColdP + kk * 8, desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
+          mma_ts(tmem + kColdK, tmem + kColdP + split_col(kk), desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar[kQEmpty + st]);
         if (i + 1 < n) issue_dp(i + 1);
@@ -299,8 +307,11 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------------- elementwise
-    const int row = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int cb = half * 64;  // first query column of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = s.scale_log2;
     bool ok = n > 0;
     if (ok) {
@@ -308,21 +319,21 @@ __global__ void __launch_bounds__(192, 1)
       it.start(s, R);
       for (int i = 0; i < n; ++i, (i < n ? it.next(s, R) : void())) {
         const int st = i & 1;
-        const float* vl = vec + st * 256;
+        const float* vl = vec + st * 256 + cb;
         if (!mbar_wait(&bar[kQFull + st], (i >> 1) & 1, err, 901)) { ok = false; break; }
         if (!mbar_wait(&bar[kSFull], i & 1, err, 902)) { ok = false; break; }
         tc_fence_after();
-        float p[128];
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + kColS + ci * 32, r);
+        float p[64];
+        {
+          uint32_t r[64];
+          tmem_ld32(tmem + lane_off + kColS + cb, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(tmem + lane_off + kColS + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 32; ++u) p[ci * 32 + u] = __uint_as_float(r[u]);
+          for (int u = 0; u < 64; ++u) p[u] = __uint_as_float(r[u]);
         }
 #pragma unroll
-        for (int u = 0; u < 128; u += 4) {
+        for (int u = 0; u < 64; u += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(vl + u);
           p[u] = ex2(fmaf(p[u], c, -l4.x));
           p[u + 1] = ex2(fmaf(p[u + 1], c, -l4.y));
@@ -331,14 +342,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (it.diag()) {
 #pragma unroll
-          for (int u = 0; u < 128; ++u) p[u] = (u < row) ? 0.f : p[u];
+          for (int u = 0; u < 64; ++u) p[u] = (cb + u < row) ? 0.f : p[u];
         }
+        {
+          uint32_t pk[32];
 #pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) pk[u] = pack_bf16x2(p[ci * 32 + 2 * u], p[ci * 32 + 2 * u + 1]);
-          tmem_st16(tmem + lane_off + kColS + ci * 16, pk);
+          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
+          tmem_st32(tmem + lane_off + kColS + cb, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -347,9 +357,9 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&bar[kdPFull], i & 1, err, 903)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
+        for (int ci = 0; ci < 2; ++ci) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + kColdP + ci * 32, r);
+          tmem_ld32(tmem + lane_off + kColdP + cb + ci * 32, r);
           tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
@@ -360,7 +370,7 @@ __global__ void __launch_bounds__(192, 1)
             const float a1 = p[cc + 1] * (__uint_as_float(r[2 * u + 1]) - d2.y);
             pk[u] = pack_bf16x2(a0, a1);
           }
-          tmem_st16(tmem + lane_off + kColdP + ci * 16, pk);
+          tmem_st16(tmem + lane_off + kColdP + cb + ci * 16, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -382,11 +392,11 @@ __global__ void __launch_bounds__(192, 1)
       float* pv_out = acc_v + (deterministic ? R.split * slice : 0) + base;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which ? kColdK : kColdV;
+        const uint32_t col = (which ? kColdK : kColdV) + half * (D / 2);
         const float mul = which ? s.scale : 1.f;
-        float* dst = which ? pk_out : pv_out;
+        float* dst = (which ? pk_out : pv_out) + half * (D / 2);
 #pragma unroll
-        for (int ci = 0; ci < D / 32; ++ci) {
+        for (int ci = 0; ci < D / 64; ++ci) {
           uint32_t r[32];
           if (n > 0) {
             tmem_ld32(tmem + lane_off + col + ci * 32, r);
@@ -412,11 +422,11 @@ __global__ void __launch_bounds__(192, 1)
       const size_t base = (static_cast<size_t>(k) * s.Hkv + hk) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which ? kColdK : kColdV;
+        const uint32_t col = (which ? kColdK : kColdV) + half * (D / 2);
         const float mul = which ? s.scale : 1.f;
-        uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + base);
+        uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + base + half * (D / 2));
 #pragma unroll
-        for (int ci = 0; ci < D / 32; ++ci) {
+        for (int ci = 0; ci < D / 64; ++ci) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + col + ci * 32, r);
           tmem_ld_wait();
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -451,7 +461,7 @@ cudaError_t launch_dkdv_d(const Sched& s, const CUtensorMap& mQ, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hkv);
-  dkdv_kernel<D><<<grid, 192, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
+  dkdv_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
                                                    static_cast<__nv_bfloat16*>(dv), acc_k, acc_v, deterministic, err);
   return cudaGetLastError();
 }

@@ -9,8 +9,10 @@
 //   dQ += dS K,   and finally dQ *= scale.
 // A CTA is the only writer of its dQ rows, so dQ needs no atomics.
 //
-// Warp roles (192 threads): warps 0-3 elementwise (thread r = query row r),
-// warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+// Warp roles (320 threads): warps 0-7 elementwise -- warp w handles query
+// rows 32*(w%4) .. +31 (its TMEM lane quarter) and key columns 64*(w/4) .. +63,
+// so every SM sub-partition runs two elementwise warps; warp 8 TMA producer;
+// warp 9 TMEM allocator + MMA issuer.
 // TMEM columns: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16, two per
 // column) double buffer [384,448) and [448,512).
 #include <cuda_bf16.h>
@@ -51,9 +53,10 @@ enum DqBar {
 };
 
 constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 256, kColdS = 384;
+constexpr int kEwThreads = 256;
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     dq_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
               const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
               const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
@@ -73,11 +76,11 @@ __global__ void __launch_bounds__(192, 1)
   w.init(s, item);
   const int n = w.n;
 
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 256) {
     mbar_init(&bar[kQFull], 1);
     for (int i = 0; i < L::kKStages; ++i) {
       mbar_init(&bar[kKFull + i], 1);
@@ -88,11 +91,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bar[kVEmpty + i], 1);
     }
     mbar_init(&bar[kSFull], 1);
-    mbar_init(&bar[kSFree], 128);
+    mbar_init(&bar[kSFree], kEwThreads);
     mbar_init(&bar[kdPFull], 1);
-    mbar_init(&bar[kdPFree], 128);
+    mbar_init(&bar[kdPFree], kEwThreads);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[kdSFull + i], 128);
+      mbar_init(&bar[kdSFull + i], kEwThreads);
       mbar_init(&bar[kdSFree + i], 1);
     }
     fence_mbar_init();
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar[kQFull], 2 * L::kTileBytes);
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(192, 1)
         if (++vs == L::kVStages) { vs = 0; vph ^= 1; }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
@@ -186,8 +189,11 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------------- elementwise
-    const int row = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int cb = half * 64;  // first key column of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = s.scale_log2;
     const int q = w.q0 + row;
     // Rows past the segment end are never stored; give them P = 0.
@@ -201,36 +207,36 @@ __global__ void __launch_bounds__(192, 1)
       const int b = j & 1;
       if (!mbar_wait(&bar[kSFull], j & 1, err, 601)) { ok = false; break; }
       tc_fence_after();
-      float p[128];
-#pragma unroll
-      for (int ci = 0; ci < 4; ++ci) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColS + ci * 32, r);
+      float p[64];
+      {
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_off + kColS + cb, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tmem + lane_off + kColS + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p[ci * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       mbar_arrive(&bar[kSFree]);
 #pragma unroll
-      for (int i = 0; i < 128; ++i) p[i] = ex2(fmaf(p[i], c, -lse2));
+      for (int i = 0; i < 64; ++i) p[i] = ex2(fmaf(p[i], c, -lse2));
       const int mk = w.mask_kind(j);
       if (mk == 1) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) p[i] = (i > row) ? 0.f : p[i];
+        for (int i = 0; i < 64; ++i) p[i] = (cb + i > row) ? 0.f : p[i];
       } else if (mk == 2) {
-        const int lim = w.P - w.k0(j);
+        const int lim = w.P - w.k0(j) - cb;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) p[i] = (i >= lim) ? 0.f : p[i];
+        for (int i = 0; i < 64; ++i) p[i] = (i >= lim) ? 0.f : p[i];
       }
       if (!mbar_wait(&bar[kdPFull], j & 1, err, 602)) { ok = false; break; }
       tc_fence_after();
       // dS buffer b was last read by the dQ product of tile j-2.
       if (j >= 2 && !mbar_wait(&bar[kdSFree + b], ((j >> 1) - 1) & 1, err, 603)) { ok = false; break; }
 #pragma unroll
-      for (int ci = 0; ci < 4; ++ci) {
+      for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColdP + ci * 32, r);
+        tmem_ld32(tmem + lane_off + kColdP + cb + ci * 32, r);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
           const float d1 = p[ci * 32 + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - Dr);
           pk[i] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(tmem + lane_off + kColdS + b * 64 + ci * 16, pk);
+        tmem_st16(tmem + lane_off + kColdS + b * 64 + half * 32 + ci * 16, pk);
       }
       tc_fence_before();
       mbar_arrive(&bar[kdPFree]);
@@ -253,11 +259,11 @@ __global__ void __launch_bounds__(192, 1)
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const bool valid = q < w.q_end;
-      uint4* dst = reinterpret_cast<uint4*>(dq + (static_cast<size_t>(q) * s.Hq + h) * D);
+      uint4* dst = reinterpret_cast<uint4*>(dq + (static_cast<size_t>(q) * s.Hq + h) * D + half * (D / 2));
 #pragma unroll
-      for (int ci = 0; ci < D / 32; ++ci) {
+      for (int ci = 0; ci < D / 64; ++ci) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColdQ + ci * 32, r);
+        tmem_ld32(tmem + lane_off + kColdQ + half * (D / 2) + ci * 32, r);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -288,7 +294,7 @@ cudaError_t launch_dq_d(const Sched& s, const CUtensorMap& mQ, const CUtensorMap
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hq);
-  dq_kernel<D><<<grid, 192, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dq), err);
+  dq_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dq), err);
   return cudaGetLastError();
 }
 

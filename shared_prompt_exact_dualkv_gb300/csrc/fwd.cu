@@ -8,10 +8,13 @@
 // (running max and sum, FlashAttention-2 lineage named on the research-map
 // page) and the kernel writes O (bf16) and the natural-log LSE (fp32).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue; thread r owns query row r of the tile
-//   warp  4    TMA producer: Q once, then K/V tiles into a 2-stage ring
-//   warp  5    TMEM allocator and MMA issuer
+// Warp roles (320 threads):
+//   warps 0-7  softmax + epilogue; warp w owns query rows 32*(w%4) .. +31 (its
+//              TMEM lane quarter) and key columns 64*(w/4) .. +63 of each S
+//              tile, so every row is shared by two threads that swap their
+//              partial row maxima through shared memory once per key tile
+//   warp  8    TMA producer: Q once, then K/V tiles into 2-stage rings
+//   warp  9    TMEM allocator and MMA issuer
 // TMEM columns: S double buffer [0,128) and [128,256), O [256,256+D),
 // P (bf16, two per column) [384,448).
 #include <cuda_bf16.h>
@@ -30,7 +33,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kX = kV + kStages * kTileBytes;  // row-max exchange [2][2][128] + row sums [2][128]
+  static constexpr int kBar = kX + 3072;
   static constexpr int kBytes = kBar + 256 + 1024;  // barriers, TMEM slot, alignment slack
 };
 
@@ -44,13 +48,16 @@ enum FwdBar {
   kSFree = 11,    // + buffer
   kPFull = 13,
   kODone = 14,
-  kNumFwdBars = 15
+  kXch = 15,      // + tile parity: both halves of every row posted their max
+  kLx = 17,       // both halves posted their row sums
+  kNumFwdBars = 18
 };
 
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384;
+constexpr int kSmThreads = 256;  // softmax threads (two per query row)
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                __nv_bfloat16* __restrict__ out, float* __restrict__ lse, unsigned int* err) {
@@ -58,7 +65,7 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 192);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -69,11 +76,11 @@ __global__ void __launch_bounds__(192, 1)
   w.init(s, item);
   const int n = w.n;
 
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 256) {
     mbar_init(&bar[kQFull], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kKFull + i], 1);
@@ -81,10 +88,12 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bar[kKEmpty + i], 1);
       mbar_init(&bar[kVEmpty + i], 1);
       mbar_init(&bar[kSFull + i], 1);
-      mbar_init(&bar[kSFree + i], 128);
+      mbar_init(&bar[kSFree + i], kSmThreads);
+      mbar_init(&bar[kXch + i], kSmThreads);
     }
-    mbar_init(&bar[kPFull], 128);
+    mbar_init(&bar[kPFull], kSmThreads);
     mbar_init(&bar[kODone], 1);
+    mbar_init(&bar[kLx], kSmThreads);
     fence_mbar_init();
     tma_prefetch_desc(&mQ);
     tma_prefetch_desc(&mK);
@@ -95,7 +104,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar[kQFull], L::kTileBytes);
@@ -113,7 +122,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
@@ -155,27 +164,30 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    const int row = threadIdx.x;  // 0..127
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int cb = half * 64;  // first key column of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float* xmax = reinterpret_cast<float*>(sm + L::kX);  // [parity][half][row]
+    float* xsum = xmax + 512;                            // [half][row]
     const float c = s.scale_log2;
     float m_use = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;  // this thread's share of the row sum
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&bar[kSFull + b], (j >> 1) & 1, err, 301)) { ok = false; break; }
       tc_fence_after();
-      float x[128];
+      float x[64];
       {
-        const uint32_t tS = tmem + lane_off + (b ? kColS1 : kColS0);
+        const uint32_t tS = tmem + lane_off + (b ? kColS1 : kColS0) + cb;
+        uint32_t r[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld_wait();
 #pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-          uint32_t r[32];
-          tmem_ld32(tS + ci * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[ci * 32 + i] = __uint_as_float(r[i]);
-        }
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       mbar_arrive(&bar[kSFree + b]);
@@ -183,18 +195,23 @@ __global__ void __launch_bounds__(192, 1)
       const int mk = w.mask_kind(j);
       if (mk == 1) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] = (i > row) ? -INFINITY : x[i];
+        for (int i = 0; i < 64; ++i) x[i] = (cb + i > row) ? -INFINITY : x[i];
       } else if (mk == 2) {
-        const int lim = w.P - w.k0(j);
+        const int lim = w.P - w.k0(j) - cb;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] = (i >= lim) ? -INFINITY : x[i];
+        for (int i = 0; i < 64; ++i) x[i] = (i >= lim) ? -INFINITY : x[i];
       }
       float mx[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) mx[a] = x[a];
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // row maximum over both halves of the tile
+      xmax[(b * 2 + half) * 128 + row] = mt;
+      mbar_arrive(&bar[kXch + b]);
+      if (!mbar_wait(&bar[kXch + b], (j >> 1) & 1, err, 304)) { ok = false; break; }
+      mt = fmaxf(mt, xmax[(b * 2 + (half ^ 1)) * 128 + row]);
       const float m_cand = mt * c;
       // Keep the running maximum unless it grows by more than 2^8: the final
       // normalisation is exact for any reference value, and skipping the
@@ -203,10 +220,10 @@ __global__ void __launch_bounds__(192, 1)
       const float m_new = resc ? m_cand : m_use;
       const float alpha = resc ? ex2(m_use - m_new) : 1.f;
       const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-      uint32_t p[64];
+      uint32_t p[32];
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
+      for (int i = 0; i < 32; ++i) {
         const float e0 = ex2(fmaf(x[2 * i], c, -m_sub));
         const float e1 = ex2(fmaf(x[2 * i + 1], c, -m_sub));
         rs[i & 3] += e0 + e1;
@@ -217,9 +234,9 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&bar[kODone], (j - 1) & 1, err, 302)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, resc)) {
-          const uint32_t tO = tmem + lane_off + kColO;
+          const uint32_t tO = tmem + lane_off + kColO + half * (D / 2);
 #pragma unroll
-          for (int ci = 0; ci < D / 32; ++ci) {
+          for (int ci = 0; ci < D / 64; ++ci) {
             uint32_t r[32];
             tmem_ld32(tO + ci * 32, r);
             tmem_ld_wait();
@@ -231,26 +248,28 @@ __global__ void __launch_bounds__(192, 1)
       }
       l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
       m_use = m_new;
-      {
-        const uint32_t tP = tmem + lane_off + kColP;
-        tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-        tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-      }
+      tmem_st32(tmem + lane_off + kColP + half * 32, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[kPFull]);
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bar[kODone], (n - 1) & 1, err, 303);
+    if (ok) {
+      xsum[half * 128 + row] = l;
+      mbar_arrive(&bar[kLx]);
+      ok = mbar_wait(&bar[kLx], 0, err, 305);
+      if (ok) l += xsum[(half ^ 1) * 128 + row];
+    }
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int q = w.q0 + row;
       const bool valid = q < w.q_end;
       const float inv_l = 1.f / l;
-      const uint32_t tO = tmem + lane_off + kColO;
-      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(q) * s.Hq + h) * D);
+      const uint32_t tO = tmem + lane_off + kColO + half * (D / 2);
+      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(q) * s.Hq + h) * D + half * (D / 2));
 #pragma unroll
-      for (int ci = 0; ci < D / 32; ++ci) {
+      for (int ci = 0; ci < D / 64; ++ci) {
         uint32_t r[32];
         tmem_ld32(tO + ci * 32, r);
         tmem_ld_wait();
@@ -263,13 +282,13 @@ __global__ void __launch_bounds__(192, 1)
           for (int v = 0; v < 4; ++v) dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (valid) lse[static_cast<size_t>(h) * s.T + q] = (m_use + log2f(l)) * 0.6931471805599453f;
+      if (valid && half == 0) lse[static_cast<size_t>(h) * s.T + q] = (m_use + log2f(l)) * 0.6931471805599453f;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -286,7 +305,7 @@ static cudaError_t launch_fwd_d(const Sched& s, const CUtensorMap& mQ, const CUt
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hq);
-  fwd_kernel<D><<<grid, 192, L::kBytes, stream>>>(s, mQ, mK, mV, static_cast<__nv_bfloat16*>(out), lse, err);
+  fwd_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, static_cast<__nv_bfloat16*>(out), lse, err);
   return cudaGetLastError();
 }
 
