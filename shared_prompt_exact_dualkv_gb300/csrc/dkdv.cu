@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (n > 0) {
-      if (lane == 0) {
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bar[kKVFull], 2 * L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) {
           tma_load_3d(sm + L::kK + a * 16384, &mK, &bar[kKVFull], a * 64, hk, R.k0);
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(320, 1)
           vl[128 + cidx] = dd;
         }
         __syncwarp();
-        if (lane == 0) {
+        if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kQFull + st], 2 * L::kTileBytes);
           for (int a = 0; a < D / 64; ++a) {
             tma_load_3d(sm + L::kQ + st * L::kTileBytes + a * 16384, &mQ, &bar[kQFull + st], a * 64, h, q0);
@@ -247,7 +247,9 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && n > 0) {
+    // The warp runs the loop converged (warp-uniform control flow and
+    // descriptors); one elected lane issues each MMA and commit.
+    if (n > 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16(128, D, false, true);
       const uint32_t sK = smem_u32(sm + L::kK);
@@ -261,9 +263,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + kColS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(sQ + off), idSS, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tmem + kColS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(sQ + off), idSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar[kSFull]);
+        if (elect_one()) mma_commit(&bar[kSFull]);
         return true;
       };
       auto issue_dp = [&](int i) {
@@ -272,9 +274,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + kColdP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sdO + off), idSS, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tmem + kColdP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sdO + off), idSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar[kdPFull]);
+        if (elect_one()) mma_commit(&bar[kdPFull]);
       };
       if (ok) {
         ok = issue_s(0);
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sdO = smem_u32(sm + L::kdO + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + kColdV, tmem + kColS + split_col(kk), desc_mnmajor_sw128(sdO + kk * 2048, 16384), idG,
+          if (elect_one()) mma_ts(tmem + kColdV, tmem + kColS + split_col(kk), desc_mnmajor_sw128(sdO + kk * 2048, 16384), idG,
                  (i > 0 || kk > 0) ? 1u : 0u);
         // the next S^T may overwrite P^T: it is issued after the dV product
         if (i + 1 < n && !issue_s(i + 1)) break;
@@ -298,12 +300,12 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sQ = smem_u32(sm + L::kQ + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + kColdK, tmem + kColdP + split_col(kk), desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
+          if (elect_one()) mma_ts(tmem + kColdK, tmem + kColdP + split_col(kk), desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar[kQEmpty + st]);
+        if (elect_one()) mma_commit(&bar[kQEmpty + st]);
         if (i + 1 < n) issue_dp(i + 1);
       }
-      mma_commit(&bar[kAccDone]);
+      if (elect_one()) mma_commit(&bar[kAccDone]);
     }
   } else {
     // ---------------------------------------------------------------- elementwise

@@ -111,30 +111,39 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar[kQFull], 2 * L::kTileBytes);
-      for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
-        tma_load_3d(sm + L::kdO + a * 16384, &mdO, &bar[kQFull], a * 64, h, w.q0);
+    // The warp runs the loop converged; one elected lane issues each copy.
+    {
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bar[kQFull], 2 * L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
+          tma_load_3d(sm + L::kdO + a * 16384, &mdO, &bar[kQFull], a * 64, h, w.q0);
+        }
       }
       int ks = 0, kph = 0, vs = 0, vph = 0;
       for (int j = 0; j < n; ++j) {
         const int k0 = w.k0(j);
         if (j >= L::kKStages && !mbar_wait(&bar[kKEmpty + ks], kph ^ 1, err, 401)) break;
-        mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sm + L::kK + ks * L::kTileBytes + a * 16384, &mK, &bar[kKFull + ks], a * 64, hk, k0);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(sm + L::kK + ks * L::kTileBytes + a * 16384, &mK, &bar[kKFull + ks], a * 64, hk, k0);
+        }
         if (j >= L::kVStages && !mbar_wait(&bar[kVEmpty + vs], vph ^ 1, err, 402)) break;
-        mbar_arrive_expect_tx(&bar[kVFull + vs], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sm + L::kV + vs * L::kTileBytes + a * 16384, &mV, &bar[kVFull + vs], a * 64, hk, k0);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bar[kVFull + vs], L::kTileBytes);
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(sm + L::kV + vs * L::kTileBytes + a * 16384, &mV, &bar[kVFull + vs], a * 64, hk, k0);
+        }
         if (++ks == L::kKStages) { ks = 0; kph ^= 1; }
         if (++vs == L::kVStages) { vs = 0; vph ^= 1; }
       }
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The warp runs the loop converged (warp-uniform control flow and
+    // descriptors); one elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16(128, D, false, true);
       const uint32_t sQ = smem_u32(sm + L::kQ);
@@ -150,9 +159,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + kColS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idSS, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tmem + kColS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar[kSFull]);
+        if (elect_one()) mma_commit(&bar[kSFull]);
         return true;
       };
       auto issue_dp = [&](int j) -> bool {
@@ -164,10 +173,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + kColdP, desc_kmajor_sw128(sdO + off), desc_kmajor_sw128(sV + off), idSS, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tmem + kColdP, desc_kmajor_sw128(sdO + off), desc_kmajor_sw128(sV + off), idSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar[kdPFull]);
-        mma_commit(&bar[kVEmpty + vs]);
+        if (elect_one()) mma_commit(&bar[kdPFull]);
+        if (elect_one()) mma_commit(&bar[kVEmpty + vs]);
         return true;
       };
       if (ok) ok = issue_s(0) && issue_dp(0);
@@ -180,11 +189,11 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ts(tmem + kColdQ, tmem + kColdS + b * 64 + kk * 8, desc_mnmajor_sw128(sK + kk * 2048, 16384), idQ,
+          if (elect_one()) mma_ts(tmem + kColdQ, tmem + kColdS + b * 64 + kk * 8, desc_mnmajor_sw128(sK + kk * 2048, 16384), idQ,
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar[kdSFree + b]);
-        mma_commit(&bar[kKEmpty + ks]);
+        if (elect_one()) mma_commit(&bar[kdSFree + b]);
+        if (elect_one()) mma_commit(&bar[kKEmpty + ks]);
       }
     }
   } else {

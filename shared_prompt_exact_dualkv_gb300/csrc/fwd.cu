@@ -106,25 +106,34 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar[kQFull], L::kTileBytes);
-      for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
+    // The warp runs the loop converged; one elected lane issues each copy.
+    {
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bar[kQFull], L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
+      }
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         const int k0 = w.k0(j);
         uint8_t* sK = sm + L::kK + st * L::kTileBytes;
         uint8_t* sV = sm + L::kV + st * L::kTileBytes;
         if (j >= 2 && !mbar_wait(&bar[kKEmpty + st], ((j >> 1) - 1) & 1, err, 101)) break;
-        mbar_arrive_expect_tx(&bar[kKFull + st], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + st], a * 64, hk, k0);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bar[kKFull + st], L::kTileBytes);
+          for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + st], a * 64, hk, k0);
+        }
         if (j >= 2 && !mbar_wait(&bar[kVEmpty + st], ((j >> 1) - 1) & 1, err, 102)) break;
-        mbar_arrive_expect_tx(&bar[kVFull + st], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bar[kVFull + st], L::kTileBytes);
+          for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
+        }
       }
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The warp runs the loop converged (warp-uniform control flow and
+    // descriptors); one elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       const uint32_t sQ = smem_u32(sm + L::kQ);
@@ -139,10 +148,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(dS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idS, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(dS, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar[kSFull + st]);
-        mma_commit(&bar[kKEmpty + st]);
+        if (elect_one()) mma_commit(&bar[kSFull + st]);
+        if (elect_one()) mma_commit(&bar[kKEmpty + st]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -155,11 +164,11 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sV = smem_u32(sm + L::kV + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, desc_mnmajor_sw128(sV + kk * 2048, 16384), idO,
+          if (elect_one()) mma_ts(tmem + kColO, tmem + kColP + kk * 8, desc_mnmajor_sw128(sV + kk * 2048, 16384), idO,
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar[kODone]);
-        mma_commit(&bar[kVEmpty + st]);
+        if (elect_one()) mma_commit(&bar[kODone]);
+        if (elect_one()) mma_commit(&bar[kVEmpty + st]);
       }
     }
   } else {
