@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 256) {
     mbar_init(&bar[kKVFull], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[kQFull + i], 1);
+      mbar_init(&bar[kQFull + i], 2);
       mbar_init(&bar[kQEmpty + i], 1);
     }
     mbar_init(&bar[kSFull], 1);
@@ -214,36 +214,57 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(sm + L::kV + a * 16384, &mV, &bar[kKVFull], a * 64, hk, R.k0);
         }
       }
+      // Each query tile's LSE/D values are read into registers one tile ahead,
+      // so their global-load latency overlaps the previous tile; a stage's
+      // full barrier takes two arrivals: the copy's expect-tx and "vectors stored".
       QIter it;
       it.start(s, R);
-      for (int i = 0; i < n; ++i, (i < n ? it.next(s, R) : void())) {
-        const int st = i & 1;
-        if (i >= 2 && !mbar_wait(&bar[kQEmpty + st], ((i >> 1) - 1) & 1, err, 701)) break;
-        const int h = it.head(R);
-        const int q0 = it.q0();
-        float* vl = vec + st * 256;
+      float l2[4], dd[4];
+      auto load_vec = [&](const QIter& t) {
+        const int h = t.head(R);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int cidx = lane * 4 + u;
-          const int q = q0 + cidx;
-          float l2 = INFINITY, dd = 0.f;
-          if (q < it.seg_end) {
-            l2 = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
-            dd = Dvec[static_cast<size_t>(h) * s.T + q];
+          const int q = t.q0() + lane * 4 + u;
+          l2[u] = INFINITY;
+          dd[u] = 0.f;
+          if (q < t.seg_end) {
+            l2[u] = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
+            dd[u] = Dvec[static_cast<size_t>(h) * s.T + q];
           }
-          vl[cidx] = l2;
-          vl[128 + cidx] = dd;
         }
-        __syncwarp();
+      };
+      load_vec(it);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&bar[kQEmpty + st], ((i >> 1) - 1) & 1, err, 701)) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kQFull + st], 2 * L::kTileBytes);
           for (int a = 0; a < D / 64; ++a) {
-            tma_load_3d(sm + L::kQ + st * L::kTileBytes + a * 16384, &mQ, &bar[kQFull + st], a * 64, h, q0);
-            tma_load_3d(sm + L::kdO + st * L::kTileBytes + a * 16384, &mdO, &bar[kQFull + st], a * 64, h, q0);
+            tma_load_3d(sm + L::kQ + st * L::kTileBytes + a * 16384, &mQ, &bar[kQFull + st], a * 64, it.head(R), it.q0());
+            tma_load_3d(sm + L::kdO + st * L::kTileBytes + a * 16384, &mdO, &bar[kQFull + st], a * 64, it.head(R), it.q0());
           }
         }
+        issued = i + 1;
+        float* vl = vec + st * 256;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          vl[lane * 4 + u] = l2[u];
+          vl[128 + lane * 4 + u] = dd[u];
+        }
         __syncwarp();
+        if (elect_one()) mbar_arrive(&bar[kQFull + st]);
+        __syncwarp();
+        if (i + 1 < n) {
+          it.next(s, R);
+          load_vec(it);
+        }
       }
+      // Before the CTA can exit, every copy this warp issued must have landed
+      // (the consumers may have stopped early on an error).
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+        mbar_wait(&bar[kQFull + (i & 1)], (i >> 1) & 1, err, 702);
+      mbar_wait(&bar[kKVFull], 0, err, 703);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(sm + L::kdO + a * 16384, &mdO, &bar[kQFull], a * 64, h, w.q0);
         }
       }
-      int ks = 0, kph = 0, vs = 0, vph = 0;
+      int ks = 0, kph = 0, vs = 0, vph = 0, k_issued = 0, v_issued = 0;
       for (int j = 0; j < n; ++j) {
         const int k0 = w.k0(j);
         if (j >= L::kKStages && !mbar_wait(&bar[kKEmpty + ks], kph ^ 1, err, 401)) break;
@@ -129,15 +129,24 @@ __global__ void __launch_bounds__(320, 1)
           for (int a = 0; a < D / 64; ++a)
             tma_load_3d(sm + L::kK + ks * L::kTileBytes + a * 16384, &mK, &bar[kKFull + ks], a * 64, hk, k0);
         }
+        k_issued = j + 1;
         if (j >= L::kVStages && !mbar_wait(&bar[kVEmpty + vs], vph ^ 1, err, 402)) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kVFull + vs], L::kTileBytes);
           for (int a = 0; a < D / 64; ++a)
             tma_load_3d(sm + L::kV + vs * L::kTileBytes + a * 16384, &mV, &bar[kVFull + vs], a * 64, hk, k0);
         }
+        v_issued = j + 1;
         if (++ks == L::kKStages) { ks = 0; kph ^= 1; }
         if (++vs == L::kVStages) { vs = 0; vph ^= 1; }
       }
+      // Before the CTA can exit, every copy this warp issued must have landed
+      // (the consumers may have stopped early on an error).
+      for (int j = (k_issued > L::kKStages ? k_issued - L::kKStages : 0); j < k_issued; ++j)
+        mbar_wait(&bar[kKFull + j % L::kKStages], (j / L::kKStages) & 1, err, 403);
+      for (int j = (v_issued > L::kVStages ? v_issued - L::kVStages : 0); j < v_issued; ++j)
+        mbar_wait(&bar[kVFull + j % L::kVStages], (j / L::kVStages) & 1, err, 404);
+      mbar_wait(&bar[kQFull], 0, err, 405);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_expect_tx(&bar[kQFull], L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + L::kQ + a * 16384, &mQ, &bar[kQFull], a * 64, h, w.q0);
       }
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         const int k0 = w.k0(j);
@@ -122,12 +123,21 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive_expect_tx(&bar[kKFull + st], L::kTileBytes);
           for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + st], a * 64, hk, k0);
         }
+        k_issued = j + 1;
         if (j >= 2 && !mbar_wait(&bar[kVEmpty + st], ((j >> 1) - 1) & 1, err, 102)) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kVFull + st], L::kTileBytes);
           for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
         }
+        v_issued = j + 1;
       }
+      // Before the CTA can exit, every copy this warp issued must have landed
+      // (the consumers may have stopped early on an error).
+      for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
+        mbar_wait(&bar[kKFull + (j & 1)], (j >> 1) & 1, err, 103);
+      for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
+        mbar_wait(&bar[kVFull + (j & 1)], (j >> 1) & 1, err, 104);
+      mbar_wait(&bar[kQFull], 0, err, 105);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
