@@ -16,7 +16,7 @@
 // Warp roles (320 threads):
 //   warps 0-3  softmax + epilogue of head A (thread r owns query row r)
 //   warps 4-7  softmax + epilogue of head B
-//   warp  8    TMA producer: both Q tiles once, then K/V tiles into 2-stage rings
+//   warp  8    TMA producer: both Q tiles once, then K and V tiles into 2-stage rings
 //   warp  9    TMEM allocator and MMA issuer
 // Producer and MMA warps run their loops converged; one elected lane issues
 // each copy, MMA and commit.
@@ -36,24 +36,25 @@ namespace {
 template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = 2;
-  static constexpr int kQ = 0;  // two Q tiles (heads A, B)
+  static constexpr int kKS = 2;  // K ring depth
+  static constexpr int kVS = 2;  // V ring depth
+  static constexpr int kQ = 0;   // two Q tiles (heads A, B)
   static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kV = kK + kKS * kTileBytes;
+  static constexpr int kBar = kV + kVS * kTileBytes;
   static constexpr int kBytes = kBar + 256 + 1024;  // barriers, TMEM slot, alignment slack
 };
 
 enum FwdBar {
   kQFull = 0,
-  kKFull = 1,     // + stage
-  kVFull = 3,     // + stage
-  kKEmpty = 5,    // + stage: released once both heads' QK^T have read it
-  kVEmpty = 7,    // + stage: released once both heads' PV have read it
-  kSFull = 9,     // + head: scores of the current key tile are in TMEM
-  kPFull = 11,    // + head: P written to TMEM (and O rescaled)
-  kODone = 13,    // + head: last PV product complete
-  kNumFwdBars = 15
+  kKFull = 1,     // + stage (3)
+  kKEmpty = 4,    // + stage: released once both heads' QK^T have read it
+  kVFull = 7,     // + stage (2)
+  kVEmpty = 9,    // + stage: released once both heads' PV have read it
+  kSFull = 11,    // + head: scores of the current key tile are in TMEM
+  kPFull = 13,    // + head: P written to TMEM (and O rescaled)
+  kODone = 15,    // + head: last PV product complete
+  kNumFwdBars = 17
 };
 
 constexpr int kHeadThreads = 128;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 192);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -145,11 +146,15 @@ __global__ void __launch_bounds__(320, 1)
   }
   if (threadIdx.x == 256) {
     mbar_init(&bar[kQFull], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < L::kKS; ++i) {
       mbar_init(&bar[kKFull + i], 1);
-      mbar_init(&bar[kVFull + i], 1);
       mbar_init(&bar[kKEmpty + i], 1);
+    }
+    for (int i = 0; i < L::kVS; ++i) {
+      mbar_init(&bar[kVFull + i], 1);
       mbar_init(&bar[kVEmpty + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kSFull + i], 1);
       mbar_init(&bar[kPFull + i], kHeadThreads);
       mbar_init(&bar[kODone + i], 1);
@@ -174,29 +179,29 @@ __global__ void __launch_bounds__(320, 1)
     }
     int k_issued = 0, v_issued = 0;
     for (int j = 0; j < n; ++j) {
-      const int st = j & 1;
+      const int ks = j % L::kKS, vs = j % L::kVS;
       const int k0 = w.k0(j);
-      uint8_t* sK = sm + L::kK + st * L::kTileBytes;
-      uint8_t* sV = sm + L::kV + st * L::kTileBytes;
-      if (j >= 2 && !mbar_wait(&bar[kKEmpty + st], ((j >> 1) - 1) & 1, err, 101)) break;
+      uint8_t* sK = sm + L::kK + ks * L::kTileBytes;
+      uint8_t* sV = sm + L::kV + vs * L::kTileBytes;
+      if (j >= L::kKS && !mbar_wait(&bar[kKEmpty + ks], ((j / L::kKS) - 1) & 1, err, 101)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bar[kKFull + st], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + st], a * 64, hk, k0);
+        mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sK + a * 16384, &mK, &bar[kKFull + ks], a * 64, hk, k0);
       }
       k_issued = j + 1;
-      if (j >= 2 && !mbar_wait(&bar[kVEmpty + st], ((j >> 1) - 1) & 1, err, 102)) break;
+      if (j >= L::kVS && !mbar_wait(&bar[kVEmpty + vs], ((j / L::kVS) - 1) & 1, err, 102)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bar[kVFull + st], L::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + st], a * 64, hk, k0);
+        mbar_arrive_expect_tx(&bar[kVFull + vs], L::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sV + a * 16384, &mV, &bar[kVFull + vs], a * 64, hk, k0);
       }
       v_issued = j + 1;
     }
     // Before the CTA can exit, every copy this warp issued must have landed
     // (the consumers may have stopped early on an error).
-    for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
-      mbar_wait(&bar[kKFull + (j & 1)], (j >> 1) & 1, err, 103);
-    for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
-      mbar_wait(&bar[kVFull + (j & 1)], (j >> 1) & 1, err, 104);
+    for (int j = (k_issued > L::kKS ? k_issued - L::kKS : 0); j < k_issued; ++j)
+      mbar_wait(&bar[kKFull + j % L::kKS], (j / L::kKS) & 1, err, 103);
+    for (int j = (v_issued > L::kVS ? v_issued - L::kVS : 0); j < v_issued; ++j)
+      mbar_wait(&bar[kVFull + j % L::kVS], (j / L::kVS) & 1, err, 104);
     mbar_wait(&bar[kQFull], 0, err, 105);
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
@@ -205,11 +210,11 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = mbar_wait(&bar[kQFull], 0, err, 201);
     // S_x(j) = Q_x K_j^T; the K stage is released after the last head's product
     auto issue_s = [&](int j, int x) -> bool {
-      const int st = j & 1;
-      if (x == 0 && !mbar_wait(&bar[kKFull + st], (j >> 1) & 1, err, 202)) return false;
+      const int ks = j % L::kKS;
+      if (x == 0 && !mbar_wait(&bar[kKFull + ks], (j / L::kKS) & 1, err, 202)) return false;
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ + x * L::kTileBytes);
-      const uint32_t sK = smem_u32(sm + L::kK + st * L::kTileBytes);
+      const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -217,23 +222,23 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tmem + col_s(x), desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(sK + off), idS, kk > 0 ? 1u : 0u);
       }
       if (elect_one()) mma_commit(&bar[kSFull + x]);
-      if (x == nheads - 1 && elect_one()) mma_commit(&bar[kKEmpty + st]);
+      if (x == nheads - 1 && elect_one()) mma_commit(&bar[kKEmpty + ks]);
       return true;
     };
     for (int x = 0; ok && x < nheads; ++x) ok = issue_s(0, x);
     for (int j = 0; ok && j < n; ++j) {
-      const int st = j & 1;
-      const uint32_t sV = smem_u32(sm + L::kV + st * L::kTileBytes);
+      const int vs = j % L::kVS;
+      const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
       for (int x = 0; ok && x < nheads; ++x) {
         if (!mbar_wait(&bar[kPFull + x], j & 1, err, 204)) { ok = false; break; }
-        if (x == 0 && !mbar_wait(&bar[kVFull + st], (j >> 1) & 1, err, 205)) { ok = false; break; }
+        if (x == 0 && !mbar_wait(&bar[kVFull + vs], (j / L::kVS) & 1, err, 205)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           if (elect_one())
             mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, desc_mnmajor_sw128(sV + kk * 2048, 16384), idO,
                    (j > 0 || kk > 0) ? 1u : 0u);
-        if (x == nheads - 1 && elect_one()) mma_commit(&bar[kVEmpty + st]);
+        if (x == nheads - 1 && elect_one()) mma_commit(&bar[kVEmpty + vs]);
         if (j + 1 < n) {
           // overwrites this head's S/P block; in issue order after the PV that reads P
           if (!issue_s(j + 1, x)) { ok = false; break; }
