@@ -358,10 +358,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int u = 0; u < 64; u += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(vl + u);
-          p[u] = ex2(fmaf(p[u], c, -l4.x));
-          p[u + 1] = ex2(fmaf(p[u + 1], c, -l4.y));
-          p[u + 2] = ex2(fmaf(p[u + 2], c, -l4.z));
-          p[u + 3] = ex2(fmaf(p[u + 3], c, -l4.w));
+          const float2 a0 = fma2(make_float2(p[u], p[u + 1]), make_float2(c, c), make_float2(-l4.x, -l4.y));
+          const float2 a1 = fma2(make_float2(p[u + 2], p[u + 3]), make_float2(c, c), make_float2(-l4.z, -l4.w));
+          p[u] = ex2(a0.x);
+          p[u + 1] = ex2(a0.y);
+          p[u + 2] = ex2(a1.x);
+          p[u + 3] = ex2(a1.y);
         }
         if (it.diag()) {
 #pragma unroll
@@ -389,9 +391,10 @@ __global__ void __launch_bounds__(320, 1)
           for (int u = 0; u < 16; ++u) {
             const int cc = ci * 32 + 2 * u;
             const float2 d2 = *reinterpret_cast<const float2*>(vl + 128 + cc);
-            const float a0 = p[cc] * (__uint_as_float(r[2 * u]) - d2.x);
-            const float a1 = p[cc + 1] * (__uint_as_float(r[2 * u + 1]) - d2.y);
-            pk[u] = pack_bf16x2(a0, a1);
+            const float2 t = add2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])),
+                                  make_float2(-d2.x, -d2.y));
+            const float2 ds = mul2(make_float2(p[cc], p[cc + 1]), t);
+            pk[u] = pack_bf16x2(ds.x, ds.y);
           }
           tmem_st16(tmem + lane_off + kColdP + cb + ci * 16, pk);
         }

@@ -237,7 +237,11 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(&bar[kSFree]);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) p[i] = ex2(fmaf(p[i], c, -lse2));
+      for (int i = 0; i < 64; i += 2) {
+        const float2 a = fma2(make_float2(p[i], p[i + 1]), make_float2(c, c), make_float2(-lse2, -lse2));
+        p[i] = ex2(a.x);
+        p[i + 1] = ex2(a.y);
+      }
       const int mk = w.mask_kind(j);
       if (mk == 1) {
 #pragma unroll
@@ -259,9 +263,10 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float d0 = p[ci * 32 + 2 * i] * (__uint_as_float(r[2 * i]) - Dr);
-          const float d1 = p[ci * 32 + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - Dr);
-          pk[i] = pack_bf16x2(d0, d1);
+          const float2 t = add2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                make_float2(-Dr, -Dr));
+          const float2 ds = mul2(make_float2(p[ci * 32 + 2 * i], p[ci * 32 + 2 * i + 1]), t);
+          pk[i] = pack_bf16x2(ds.x, ds.y);
         }
         tmem_st16(tmem + lane_off + kColdS + b * 64 + half * 32 + ci * 16, pk);
       }

@@ -79,19 +79,21 @@ __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
     tmem_ld32(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float v = (!MASKED || hc * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY;
-      mx[i & 7] = fmaxf(mx[i & 7], v);
+    for (int i = 0; i < 64; i += 2) {
+      const float v0 = (!MASKED || hc * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY;
+      const float v1 = (!MASKED || hc * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY;
+      mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], v0, v1);
     }
   }
-  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 }
 
 // P = exp2(c*S - m_sub) as bf16 written over the first 64 columns of S;
 // returns the row sum of the (unrounded) probabilities.
 template <bool MASKED>
 __device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c, float m_sub) {
-  float rs[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_sub, -m_sub);
 #pragma unroll
   for (int hc = 0; hc < 2; ++hc) {
     uint32_t r[64];
@@ -102,18 +104,19 @@ __device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c, float m_
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int cc = hc * 64 + 2 * i;
-      float e0 = ex2(fmaf(__uint_as_float(r[2 * i]), c, -m_sub));
-      float e1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub));
+      const float2 a = fma2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2);
+      float2 e = make_float2(ex2(a.x), ex2(a.y));
       if (MASKED) {
-        e0 = (cc < lim) ? e0 : 0.f;
-        e1 = (cc + 1 < lim) ? e1 : 0.f;
+        e.x = (cc < lim) ? e.x : 0.f;
+        e.y = (cc + 1 < lim) ? e.y : 0.f;
       }
-      rs[i & 3] += e0 + e1;
-      p[i] = pack_bf16x2(e0, e1);
+      rs[i & 3] = add2(rs[i & 3], e);
+      p[i] = pack_bf16x2(e.x, e.y);
     }
     tmem_st32(tS + hc * 32, p);
   }
-  return (rs[0] + rs[1]) + (rs[2] + rs[3]);
+  const float2 t = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
+  return t.x + t.y;
 }
 
 template <int D>
