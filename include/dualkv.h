@@ -24,10 +24,11 @@
  *   R_lens           : HOST array of N int32 response lengths, read during the call.
  *   Grouped-query attention: q-head h reads kv-head h / (Hq / Hkv).
  *   Accepted shapes: d in {64, 128}; Hq % Hkv == 0; 1 <= N <= 1024; P >= 0;
- *   R_i >= 0; T < 2^31; every device pointer 16-byte aligned.  T == 0 is a
- *   no-op.  P == 0 gives N independent causal sequences; N == 1 is one causal
- *   sequence of P + R_1 rows.  The number of 128-row tiles (ceil(P/128) plus
- *   sum ceil(R_i/128)) must not exceed 5600 per launch.
+ *   R_i >= 0; T < 2^31; P and every R_i at most 8388480 rows (65535 tiles of
+ *   128); every device pointer 16-byte aligned.  T == 0 is a no-op.  P == 0
+ *   gives N independent causal sequences; N == 1 is one causal sequence of
+ *   P + R_1 rows.  Work lists longer than one launch holds are split into
+ *   several launches of the same kernel on `stream`.
  *   Packed dO of a prompt row is the gradient of the shared prompt row, i.e.
  *   the sum over the N replicated sequences of that row's gradient.
  *
@@ -62,7 +63,7 @@ extern "C" {
 typedef enum {
   DUALKV_OK = 0,
   DUALKV_ERR_INVALID_ARG = 1,  /* null pointer, negative length, N out of range, T mismatch */
-  DUALKV_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, too many tiles */
+  DUALKV_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, a segment over 65535 tiles */
   DUALKV_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned */
   DUALKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
   DUALKV_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
@@ -117,6 +118,39 @@ DUALKV_API int dualkv_bwd(const void* q, const void* k, const void* v, const voi
                const float* lse, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
                int32_t Hkv, int32_t d, float softmax_scale, int deterministic, int32_t num_splits,
                void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream);
+
+/*
+ * Several prompt groups in one packed batch (research-map page, "Key
+ * results": the speedups are quoted per micro-batch size, mb=8, without
+ * saying whether it counts prompts or sequences; "Limitations": one shared
+ * prefix per micro-batch group, no prefix trees).  These calls cover a
+ * micro-batch that holds more than one prompt, each with its own responses.  The rows hold G groups one after another, group g
+ * being its prompt of P[g] rows followed by its N[g] responses:
+ *   rows = [prompt_0 ; resp_0,0 .. resp_0,N0-1 ; prompt_1 ; resp_1,0 .. ; ...]
+ * and the visibility rule of the single-group calls holds inside each group
+ * while no row sees any key of another group.  The result equals G separate
+ * single-group calls on the groups' row ranges (with dualkv_bwd's reduction
+ * mode and split count applied per group).
+ *   G        : number of groups, >= 1.
+ *   P        : HOST array of G prompt lengths (>= 0; 0 = the group's
+ *              responses are plain causal sequences).
+ *   N        : HOST array of G response counts (>= 0; 0 = a prompt alone).
+ *   R_lens   : HOST array of sum(N) response lengths, group by group (may be
+ *              NULL when sum(N) == 0).
+ *   G + sum(N) must not exceed 1040.  Every other argument, layout, ownership
+ *   rule and status code is that of the single-group call of the same name.
+ */
+DUALKV_API int dualkv_fwd_groups(const void* q, const void* k, const void* v, int32_t G, const int64_t* P,
+                                 const int32_t* N, const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                 float softmax_scale, void* out, float* lse, void* stream);
+DUALKV_API size_t dualkv_bwd_groups_workspace_bytes(int32_t G, const int64_t* P, const int32_t* N,
+                                                    const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                                    int deterministic, int32_t num_splits);
+DUALKV_API int dualkv_bwd_groups(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                 const float* lse, int32_t G, const int64_t* P, const int32_t* N,
+                                 const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale,
+                                 int deterministic, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                 void* dq, void* dk, void* dv, void* stream);
 
 /*
  * Backward pass without any allocation (the DualKV pages have no counterpart;

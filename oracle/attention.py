@@ -194,6 +194,82 @@ def dualkv_backward(q, k, v, dout, P: int, R_lens: Sequence[int], scale: float,
 
 
 # ---------------------------------------------------------------------------
+# Several prompt groups in one packed batch (research-map page, "Limitations":
+# one shared prefix per micro-batch group; "Key results" quotes a micro-batch
+# size, mb=8, that may hold more than one prompt).  Group g occupies its own consecutive rows [prompt_g ; responses_g]
+# and no row sees a key of another group, so each group is the single-group
+# problem above on its own row range.
+# ---------------------------------------------------------------------------
+
+def group_row_starts(groups) -> list:
+    """First packed row of each group and, last, the total row count.
+
+    ``groups`` lists (P_g, R_lens_g) in row order."""
+    starts = [0]
+    for P_g, R_g in groups:
+        starts.append(starts[-1] + int(P_g) + sum(int(r) for r in R_g))
+    return starts
+
+
+def dualkv_forward_groups(q, k, v, groups, scale: float, heads: Optional[Sequence[int]] = None):
+    """Packed forward over several groups; a group without responses is its
+    prompt alone under plain causal attention."""
+    T, Hq, d = q.shape
+    starts = group_row_starts(groups)
+    if starts[-1] != T:
+        raise ValueError("row count does not match the groups")
+    g = Hq // k.shape[1]
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    lse = np.zeros((Hq, T), dtype=np.float64)
+    for (P_g, R_g), a, b in zip(groups, starts[:-1], starts[1:]):
+        if a == b:
+            continue
+        if len(R_g) == 0:
+            for h in (range(Hq) if heads is None else heads):
+                o_h, l_h = causal_attention_fwd(q[a:b, h], k[a:b, h // g], v[a:b, h // g], scale)
+                out[a:b, h] = o_h
+                lse[h, a:b] = l_h
+            continue
+        o_g, l_g = dualkv_forward(q[a:b], k[a:b], v[a:b], int(P_g), list(R_g), scale, heads=heads)
+        out[a:b] = o_g
+        lse[:, a:b] = l_g
+    return out, lse
+
+
+def dualkv_backward_groups(q, k, v, dout, groups, scale: float, heads: Optional[Sequence[int]] = None):
+    """Packed backward over several groups (prompt-row gradients summed over
+    the group's own responses only)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    starts = group_row_starts(groups)
+    if starts[-1] != T:
+        raise ValueError("row count does not match the groups")
+    g = Hq // Hkv
+    dq = np.zeros((T, Hq, d), dtype=np.float64)
+    dk = np.zeros((T, Hkv, d), dtype=np.float64)
+    dv = np.zeros((T, Hkv, d), dtype=np.float64)
+    for (P_g, R_g), a, b in zip(groups, starts[:-1], starts[1:]):
+        if a == b:
+            continue
+        if len(R_g) == 0:
+            for h in (range(Hq) if heads is None else heads):
+                j = h // g
+                o_h, l_h = causal_attention_fwd(q[a:b, h], k[a:b, j], v[a:b, j], scale)
+                dq_h, dk_h, dv_h = causal_attention_bwd(q[a:b, h], k[a:b, j], v[a:b, j], o_h, l_h,
+                                                        dout[a:b, h], scale)
+                dq[a:b, h] += dq_h
+                dk[a:b, j] += dk_h
+                dv[a:b, j] += dv_h
+            continue
+        dq_g, dk_g, dv_g = dualkv_backward(q[a:b], k[a:b], v[a:b], dout[a:b], int(P_g), list(R_g), scale,
+                                           heads=heads)
+        dq[a:b] = dq_g
+        dk[a:b] = dk_g
+        dv[a:b] = dv_g
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
 # Row-sampled oracle for full-size workloads.  The same definition, evaluated
 # one query row at a time: row t of head h sees keys [0, t] if t is a prompt
 # row, and [0, P) plus [off_i, t] if t is in response i.  Used where the

@@ -45,46 +45,99 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// Packed batch shape: G prompt groups, group g = prompt of P[g] rows then
+// N[g] responses (lengths in R, concatenated over groups).
 struct Shape {
   int64_t T = 0;
-  int32_t P = 0, N = 0, Hq = 0, Hkv = 0, d = 0;
-  std::vector<int32_t> R;
+  int32_t Hq = 0, Hkv = 0, d = 0;
+  std::vector<int32_t> P, N, R;
+  int64_t total_P = 0;
 };
 
-int check_shape(Shape* sh, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d) {
-  if (N < 1 || N > kMaxSeq || R_lens == nullptr || P < 0 || Hq < 1 || Hkv < 1) return DUALKV_ERR_INVALID_ARG;
+int check_dims(int32_t Hq, int32_t Hkv, int32_t d) {
+  if (Hq < 1 || Hkv < 1) return DUALKV_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DUALKV_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return DUALKV_ERR_UNSUPPORTED;
-  int64_t T = P;
-  sh->R.resize(N);
-  for (int i = 0; i < N; ++i) {
+  return DUALKV_OK;
+}
+
+int check_groups(Shape* sh, int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens, int32_t Hq,
+                 int32_t Hkv, int32_t d) {
+  if (G < 1 || !P || !N) return DUALKV_ERR_INVALID_ARG;
+  int64_t nres = 0;
+  for (int g = 0; g < G; ++g) {
+    if (N[g] < 0 || P[g] < 0 || P[g] >= (int64_t(1) << 31)) return DUALKV_ERR_INVALID_ARG;
+    nres += N[g];
+  }
+  if (G + nres > kMaxSeg) return DUALKV_ERR_INVALID_ARG;
+  if (nres > 0 && !R_lens) return DUALKV_ERR_INVALID_ARG;
+  const int st = check_dims(Hq, Hkv, d);
+  if (st != DUALKV_OK) return st;
+  sh->P.assign(G, 0);
+  sh->N.assign(G, 0);
+  sh->R.assign(static_cast<size_t>(nres), 0);
+  int64_t T = 0, tp = 0;
+  for (int g = 0; g < G; ++g) {
+    sh->P[g] = static_cast<int32_t>(P[g]);
+    sh->N[g] = N[g];
+    T += P[g];
+    tp += P[g];
+  }
+  // a segment's tile index has 16 bits in a work item
+  constexpr int64_t kMaxSegRows = int64_t(0xFFFF) * kTile;
+  for (int g = 0; g < G; ++g)
+    if (P[g] > kMaxSegRows) return DUALKV_ERR_UNSUPPORTED;
+  for (int64_t i = 0; i < nres; ++i) {
     if (R_lens[i] < 0) return DUALKV_ERR_INVALID_ARG;
+    if (R_lens[i] > kMaxSegRows) return DUALKV_ERR_UNSUPPORTED;
     sh->R[i] = R_lens[i];
     T += R_lens[i];
   }
-  if (T >= (int64_t(1) << 31) || T * int64_t(Hq) * d >= (int64_t(1) << 40)) return DUALKV_ERR_INVALID_ARG;
+  if (T >= (int64_t(1) << 31)) return DUALKV_ERR_INVALID_ARG;
   sh->T = T;
-  sh->P = static_cast<int32_t>(P);
-  sh->N = N;
+  sh->total_P = tp;
   sh->Hq = Hq;
   sh->Hkv = Hkv;
   sh->d = d;
   return DUALKV_OK;
 }
 
+// One group of N responses (the original single-prompt interface).
+int check_shape(Shape* sh, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (N < 1 || N > 1024 || R_lens == nullptr || P < 0) return DUALKV_ERR_INVALID_ARG;
+  return check_groups(sh, 1, &P, &N, R_lens, Hq, Hkv, d);
+}
+
+// Segments in packed order, their group info and the prompt accumulator rows.
 void fill_common(Sched* s, const Shape& sh, float scale) {
   s->T = static_cast<int32_t>(sh.T);
-  s->P = sh.P;
-  s->N = sh.N;
   s->Hq = sh.Hq;
   s->Hkv = sh.Hkv;
   s->group = sh.Hq / sh.Hkv;
   s->scale = scale;
   s->scale_log2 = scale * 1.4426950408889634f;
-  s->off[0] = sh.P;
-  for (int i = 0; i < sh.N; ++i) s->off[i + 1] = s->off[i] + sh.R[i];
   s->num_splits = 1;
   s->num_items = 0;
+  int seg = 0, r = 0;
+  int32_t row = 0, acc = 0;
+  for (size_t g = 0; g < sh.P.size(); ++g) {
+    const int p = seg;
+    s->off[seg] = row;
+    s->info[seg] = p | (sh.N[g] << 16);
+    s->acc_row[seg] = acc;
+    row += sh.P[g];
+    acc += sh.P[g];
+    ++seg;
+    for (int i = 0; i < sh.N[g]; ++i, ++r, ++seg) {
+      s->off[seg] = row;
+      s->info[seg] = p;
+      s->acc_row[seg] = 0;
+      row += sh.R[r];
+    }
+  }
+  s->off[seg] = row;
+  s->nseg = seg;
+  s->acc_rows = acc;
 }
 
 struct CostItem {
@@ -92,77 +145,78 @@ struct CostItem {
   uint32_t item;
 };
 
-int finish_items(Sched* s, std::vector<CostItem>& v) {
-  if (v.size() > static_cast<size_t>(kMaxItems)) return DUALKV_ERR_UNSUPPORTED;
+std::vector<uint32_t> sorted_items(std::vector<CostItem>& v) {
   std::stable_sort(v.begin(), v.end(), [](const CostItem& a, const CostItem& b) { return a.cost > b.cost; });
-  for (size_t i = 0; i < v.size(); ++i) s->items[i] = v[i].item;
-  s->num_items = static_cast<int32_t>(v.size());
-  return DUALKV_OK;
+  std::vector<uint32_t> out(v.size());
+  for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].item;
+  return out;
 }
 
 // Query-tile items (forward and dQ): cost = number of key tiles walked.
-int build_query_sched(Sched* s, const Shape& sh, float scale) {
-  fill_common(s, sh, scale);
+std::vector<uint32_t> query_items(const Sched& s) {
   std::vector<CostItem> v;
-  const int nP = ceil_div(sh.P, kTile);
-  for (int t = 0; t < nP; ++t) v.push_back({t + 1, make_item(t, 0, 0)});
-  for (int i = 0; i < sh.N; ++i) {
-    const int nR = ceil_div(sh.R[i], kTile);
-    for (int t = 0; t < nR; ++t) v.push_back({nP + t + 1, make_item(t, i + 1, 0)});
+  for (int seg = 0; seg < s.nseg; ++seg) {
+    const int p = s.prompt_of(seg);
+    const int nt = s.seg_tiles(seg);
+    const int nA = (p == seg) ? 0 : s.seg_tiles(p);
+    for (int t = 0; t < nt; ++t) v.push_back({nA + t + 1, make_item(t, seg, 0)});
   }
-  return finish_items(s, v);
+  return sorted_items(v);
 }
 
-// Sequence chunk boundaries of the prompt key tiles' work: split c covers
-// responses [c*N/S, (c+1)*N/S); split 0 also takes the prompt's own queries.
-int64_t prompt_item_cost(const Shape& sh, int j, int c, int S, const std::vector<int>& nR) {
-  const int nP = ceil_div(sh.P, kTile);
-  int64_t cost = (c == 0) ? (nP - j) : 0;
-  for (int i = (c * sh.N) / S; i < ((c + 1) * sh.N) / S; ++i) cost += nR[i];
-  return cost;
+// Sequence chunks of a prompt key tile's work: split c of group g covers its
+// responses [c*N_g/S, (c+1)*N_g/S); split 0 also takes the prompt's own queries.
+std::vector<uint32_t> key_items(const Sched& s, int S) {
+  std::vector<CostItem> v;
+  for (int seg = 0; seg < s.nseg; ++seg) {
+    const int nt = s.seg_tiles(seg);
+    if (s.prompt_of(seg) == seg) {
+      // Every (prompt key tile, split) is listed, even one whose sequence chunk
+      // has no query tiles: in deterministic mode it must still write its
+      // (zero) partial slice, which the fixed-order reduce reads.
+      const int ng = s.responses_of(seg);
+      for (int j = 0; j < nt; ++j)
+        for (int c = 0; c < S; ++c) {
+          int64_t cost = (c == 0) ? (nt - j) : 0;
+          for (int i = seg + 1 + (c * ng) / S; i < seg + 1 + ((c + 1) * ng) / S; ++i) cost += s.seg_tiles(i);
+          v.push_back({cost, make_item(j, seg, c)});
+        }
+    } else {
+      for (int j = 0; j < nt; ++j) v.push_back({nt - j, make_item(j, seg, 0)});
+    }
+  }
+  return sorted_items(v);
 }
 
 int auto_splits(const Shape& sh) {
-  const int nP = ceil_div(sh.P, kTile);
-  if (nP == 0) return 1;
-  std::vector<int> nR(sh.N);
-  int64_t resp_tiles = 0, total = 0;
-  for (int i = 0; i < sh.N; ++i) {
-    nR[i] = ceil_div(sh.R[i], kTile);
-    resp_tiles += nR[i];
-    total += int64_t(nR[i]) * (nR[i] + 1) / 2;  // response key tiles
+  int64_t total = 0, biggest = 0;
+  int maxN = 1;
+  size_t r = 0;
+  for (size_t g = 0; g < sh.P.size(); ++g) {
+    const int nP = ceil_div(sh.P[g], kTile);
+    int64_t resp_tiles = 0;
+    for (int i = 0; i < sh.N[g]; ++i, ++r) {
+      const int nR = ceil_div(sh.R[r], kTile);
+      resp_tiles += nR;
+      total += int64_t(nR) * (nR + 1) / 2;
+    }
+    total += int64_t(nP) * (nP + 1) / 2 + int64_t(nP) * resp_tiles;
+    if (nP > 0) biggest = std::max<int64_t>(biggest, nP + resp_tiles);
+    maxN = std::max(maxN, sh.N[g]);
   }
-  total += int64_t(nP) * (nP + 1) / 2 + int64_t(nP) * resp_tiles;  // prompt key tiles
+  if (biggest == 0) return 1;
   total *= sh.Hkv;
   // Largest single item at most a quarter of one SM's fair share.
   const double target = std::max(1.0, double(total) / (4.0 * num_sms()));
-  const double biggest = double(nP + resp_tiles);
-  int S = static_cast<int>(std::ceil(biggest / target));
-  S = std::max(1, std::min({S, sh.N, 16}));
-  return S;
-}
-
-// Key-tile items (dK/dV): cost = number of query tiles walked per q-head.
-int build_key_sched(Sched* s, const Shape& sh, float scale, int S) {
-  fill_common(s, sh, scale);
-  s->num_splits = S;
-  std::vector<CostItem> v;
-  std::vector<int> nR(sh.N);
-  for (int i = 0; i < sh.N; ++i) nR[i] = ceil_div(sh.R[i], kTile);
-  const int nP = ceil_div(sh.P, kTile);
-  // Every (prompt key tile, split) is listed, even one whose sequence chunk
-  // has no query tiles: in deterministic mode it must still write its
-  // (zero) partial slice, which the fixed-order reduce reads.
-  for (int j = 0; j < nP; ++j)
-    for (int c = 0; c < S; ++c) v.push_back({prompt_item_cost(sh, j, c, S, nR), make_item(j, 0, c)});
-  for (int i = 0; i < sh.N; ++i)
-    for (int j = 0; j < nR[i]; ++j) v.push_back({nR[i] - j, make_item(j, i + 1, 0)});
-  return finish_items(s, v);
+  int S = static_cast<int>(std::ceil(double(biggest) / target));
+  return std::max(1, std::min({S, maxN, 16}));
 }
 
 int resolve_splits(const Shape& sh, int32_t num_splits) {
   if (num_splits <= 0) return auto_splits(sh);
-  return std::max(1, std::min({num_splits, sh.N, 31}));
+  int maxN = 1;
+  for (int n : sh.N) maxN = std::max(maxN, n);
+  return std::max(1, std::min({num_splits, maxN, 31}));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -177,13 +231,26 @@ struct WsLayout {
 WsLayout workspace_layout(const Shape& sh, int deterministic, int S) {
   WsLayout w;
   w.S = S;
-  w.slice = size_t(sh.P) * sh.Hkv * sh.d;
+  w.slice = size_t(sh.total_P) * sh.Hkv * sh.d;
   w.acc_floats = deterministic ? w.slice * S : w.slice;
   w.D = 0;
   w.acc_k = align256(size_t(sh.T) * sh.Hq * 4);
   w.acc_v = w.acc_k + align256(w.acc_floats * 4);
   w.total = w.acc_v + align256(w.acc_floats * 4);
   return w;
+}
+
+// Launches `launch` once per chunk of at most kMaxItems items.
+template <typename F>
+cudaError_t launch_chunks(Sched* s, const std::vector<uint32_t>& items, F&& launch) {
+  for (size_t i0 = 0; i0 < items.size(); i0 += kMaxItems) {
+    const size_t n = std::min(items.size() - i0, static_cast<size_t>(kMaxItems));
+    std::copy(items.begin() + i0, items.begin() + i0 + n, s->items);
+    s->num_items = static_cast<int32_t>(n);
+    const cudaError_t e = launch(*s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : DUALKV_ERR_CUDA; }
@@ -242,6 +309,107 @@ struct TraceScope {
   }
 };
 
+PromptMap* make_prompt_map(const Shape& sh) {
+  PromptMap* m = new PromptMap;
+  m->ngroups = 0;
+  int64_t row = 0, acc = 0;
+  size_t r = 0;
+  for (size_t g = 0; g < sh.P.size(); ++g) {
+    if (sh.P[g] > 0) {
+      m->acc_row[m->ngroups] = static_cast<int32_t>(acc);
+      m->packed_row[m->ngroups] = static_cast<int32_t>(row);
+      ++m->ngroups;
+    }
+    row += sh.P[g];
+    acc += sh.P[g];
+    for (int i = 0; i < sh.N[g]; ++i, ++r) row += sh.R[r];
+  }
+  m->acc_row[m->ngroups] = static_cast<int32_t>(acc);
+  return m;
+}
+
+int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float scale, void* out, float* lse,
+             void* stream) {
+  if (!std::isfinite(scale)) return DUALKV_ERR_INVALID_ARG;
+  if (sh.T == 0) return DUALKV_OK;
+  if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return DUALKV_ERR_ALIGNMENT;
+  std::unique_ptr<Sched> s(new Sched);
+  fill_common(s.get(), sh, scale);
+  const std::vector<uint32_t> items = query_items(*s);
+  CUtensorMap mQ, mK, mV;
+  if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
+      !make_map_thd(&mV, v, sh.T, sh.Hkv, sh.d, kTile))
+    return DUALKV_ERR_CUDA;
+  unsigned int* err = error_word_ptr();
+  if (!err) return DUALKV_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return map_cuda(launch_chunks(s.get(), items, [&](const Sched& c) {
+    TraceScope ts(0, cs);
+    return launch_fwd(c, sh.d, mQ, mK, mV, out, lse, err, cs);
+  }));
+}
+
+int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, float scale, int deterministic, int32_t num_splits, void* workspace,
+             size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream) {
+  if (!std::isfinite(scale)) return DUALKV_ERR_INVALID_ARG;
+  if (sh.T == 0) return DUALKV_OK;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return DUALKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return DUALKV_ERR_ALIGNMENT;
+  const int det = deterministic ? 1 : 0;
+  const int S = resolve_splits(sh, num_splits);
+  const WsLayout ws = workspace_layout(sh, det, S);
+  if (!workspace || workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DUALKV_ERR_ALIGNMENT;
+
+  std::unique_ptr<Sched> sq(new Sched), sk(new Sched);
+  fill_common(sq.get(), sh, scale);
+  fill_common(sk.get(), sh, scale);
+  sk->num_splits = S;
+  const std::vector<uint32_t> q_items = query_items(*sq);
+  const std::vector<uint32_t> k_items = key_items(*sk, S);
+  std::unique_ptr<PromptMap> map(make_prompt_map(sh));
+  CUtensorMap mQ, mK, mV, mdO;
+  if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
+      !make_map_thd(&mV, v, sh.T, sh.Hkv, sh.d, kTile) || !make_map_thd(&mdO, dout, sh.T, sh.Hq, sh.d, kTile))
+    return DUALKV_ERR_CUDA;
+  unsigned int* err = error_word_ptr();
+  if (!err) return DUALKV_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* wb = static_cast<uint8_t*>(workspace);
+  float* Dvec = reinterpret_cast<float*>(wb + ws.D);
+  float* acc_k = reinterpret_cast<float*>(wb + ws.acc_k);
+  float* acc_v = reinterpret_cast<float*>(wb + ws.acc_v);
+
+  cudaError_t e;
+  {
+    TraceScope ts(1, cs);
+    // the atomic mode accumulates into acc_k/acc_v, which start at zero;
+    // the deterministic mode overwrites every slice it reads
+    e = launch_preprocess(out, dout, Dvec, sh.T, sh.Hq, sh.d, det ? nullptr : acc_k,
+                          det ? 0 : (ws.total - ws.acc_k) / 4, cs);
+  }
+  if (e == cudaSuccess)
+    e = launch_chunks(sk.get(), k_items, [&](const Sched& c) {
+      TraceScope ts(2, cs);
+      return launch_dkdv(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, det, err, cs);
+    });
+  if (e == cudaSuccess && map->ngroups > 0) {
+    TraceScope ts(3, cs);
+    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, *map, sh.Hkv * sh.d, cs);
+  }
+  if (e == cudaSuccess)
+    e = launch_chunks(sq.get(), q_items, [&](const Sched& c) {
+      TraceScope ts(4, cs);
+      return launch_dq(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dq, err, cs);
+    });
+  return map_cuda(e);
+}
+
 }  // namespace
 }  // namespace dkv
 
@@ -255,7 +423,7 @@ const char* dualkv_status_string(int status) {
   switch (status) {
     case DUALKV_OK: return "ok";
     case DUALKV_ERR_INVALID_ARG: return "invalid argument";
-    case DUALKV_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, Hq % Hkv == 0, tile count within limit)";
+    case DUALKV_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, Hq % Hkv == 0, each prompt or response at most 8388480 rows)";
     case DUALKV_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
     case DUALKV_ERR_WORKSPACE: return "workspace missing or too small";
     case DUALKV_ERR_CUDA: return "CUDA runtime or launch error";
@@ -267,32 +435,33 @@ const char* dualkv_status_string(int status) {
 int dualkv_fwd(const void* q, const void* k, const void* v, int64_t P, int32_t N, const int32_t* R_lens,
                int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale, void* out, float* lse, void* stream) {
   Shape sh;
-  int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
+  const int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
   if (st != DUALKV_OK) return st;
-  if (!std::isfinite(softmax_scale)) return DUALKV_ERR_INVALID_ARG;
-  if (sh.T == 0) return DUALKV_OK;
-  if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
-    return DUALKV_ERR_ALIGNMENT;
-  std::unique_ptr<Sched> s(new Sched);
-  st = build_query_sched(s.get(), sh, softmax_scale);
+  return fwd_impl(sh, q, k, v, softmax_scale, out, lse, stream);
+}
+
+int dualkv_fwd_groups(const void* q, const void* k, const void* v, int32_t G, const int64_t* P, const int32_t* N,
+                      const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale, void* out,
+                      float* lse, void* stream) {
+  Shape sh;
+  const int st = check_groups(&sh, G, P, N, R_lens, Hq, Hkv, d);
   if (st != DUALKV_OK) return st;
-  CUtensorMap mQ, mK, mV;
-  if (!make_map_thd(&mQ, q, sh.T, Hq, d, kTile) || !make_map_thd(&mK, k, sh.T, Hkv, d, kTile) ||
-      !make_map_thd(&mV, v, sh.T, Hkv, d, kTile))
-    return DUALKV_ERR_CUDA;
-  unsigned int* err = error_word_ptr();
-  if (!err) return DUALKV_ERR_CUDA;
-  TraceScope ts(0, static_cast<cudaStream_t>(stream));
-  return map_cuda(launch_fwd(*s, d, mQ, mK, mV, out, lse, err, static_cast<cudaStream_t>(stream)));
+  return fwd_impl(sh, q, k, v, softmax_scale, out, lse, stream);
 }
 
 size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq, int32_t Hkv,
                                   int32_t d, int deterministic, int32_t num_splits) {
   Shape sh;
   if (check_shape(&sh, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK) return 0;
-  const int S = resolve_splits(sh, num_splits);
-  return workspace_layout(sh, deterministic ? 1 : 0, S).total;
+  return workspace_layout(sh, deterministic ? 1 : 0, resolve_splits(sh, num_splits)).total;
+}
+
+size_t dualkv_bwd_groups_workspace_bytes(int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens,
+                                         int32_t Hq, int32_t Hkv, int32_t d, int deterministic,
+                                         int32_t num_splits) {
+  Shape sh;
+  if (check_groups(&sh, G, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK) return 0;
+  return workspace_layout(sh, deterministic ? 1 : 0, resolve_splits(sh, num_splits)).total;
 }
 
 int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
@@ -300,56 +469,22 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
                float softmax_scale, int deterministic, int32_t num_splits, void* workspace,
                size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream) {
   Shape sh;
-  int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
+  const int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
   if (st != DUALKV_OK) return st;
-  if (!std::isfinite(softmax_scale)) return DUALKV_ERR_INVALID_ARG;
-  if (sh.T == 0) return DUALKV_OK;
-  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return DUALKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return DUALKV_ERR_ALIGNMENT;
-  const int det = deterministic ? 1 : 0;
-  const int S = resolve_splits(sh, num_splits);
-  const WsLayout ws = workspace_layout(sh, det, S);
-  if (!workspace || workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DUALKV_ERR_ALIGNMENT;
+  return bwd_impl(sh, q, k, v, out, dout, lse, softmax_scale, deterministic, num_splits, workspace,
+                  workspace_bytes, dq, dk, dv, stream);
+}
 
-  std::unique_ptr<Sched> sq(new Sched), sk(new Sched);
-  st = build_query_sched(sq.get(), sh, softmax_scale);
+int dualkv_bwd_groups(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens,
+                      int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale, int deterministic,
+                      int32_t num_splits, void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv,
+                      void* stream) {
+  Shape sh;
+  const int st = check_groups(&sh, G, P, N, R_lens, Hq, Hkv, d);
   if (st != DUALKV_OK) return st;
-  st = build_key_sched(sk.get(), sh, softmax_scale, S);
-  if (st != DUALKV_OK) return st;
-  CUtensorMap mQ, mK, mV, mdO;
-  if (!make_map_thd(&mQ, q, sh.T, Hq, d, kTile) || !make_map_thd(&mK, k, sh.T, Hkv, d, kTile) ||
-      !make_map_thd(&mV, v, sh.T, Hkv, d, kTile) || !make_map_thd(&mdO, dout, sh.T, Hq, d, kTile))
-    return DUALKV_ERR_CUDA;
-  unsigned int* err = error_word_ptr();
-  if (!err) return DUALKV_ERR_CUDA;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  uint8_t* wb = static_cast<uint8_t*>(workspace);
-  float* Dvec = reinterpret_cast<float*>(wb + ws.D);
-  float* acc_k = reinterpret_cast<float*>(wb + ws.acc_k);
-  float* acc_v = reinterpret_cast<float*>(wb + ws.acc_v);
-
-  cudaError_t e;
-  {
-    TraceScope ts(1, cs);
-    e = launch_preprocess(out, dout, Dvec, sh.T, Hq, d, det ? nullptr : acc_k,
-                          det ? 0 : 2 * (ws.acc_v - ws.acc_k) / 4, cs);
-  }
-  if (e == cudaSuccess) {
-    TraceScope ts(2, cs);
-    e = launch_dkdv(*sk, d, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, det, err, cs);
-  }
-  if (e == cudaSuccess && sh.P > 0) {
-    TraceScope ts(3, cs);
-    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, ws.slice, cs);
-  }
-  if (e == cudaSuccess) {
-    TraceScope ts(4, cs);
-    e = launch_dq(*sq, d, mQ, mK, mV, mdO, lse, Dvec, dq, err, cs);
-  }
-  return map_cuda(e);
+  return bwd_impl(sh, q, k, v, out, dout, lse, softmax_scale, deterministic, num_splits, workspace,
+                  workspace_bytes, dq, dk, dv, stream);
 }
 
 int dualkv_trace_enable(int on) {

@@ -71,35 +71,38 @@ __device__ __forceinline__ uint32_t split_col(int kk) { return kk < 4 ? kk * 8 :
 // of one segment; the walk repeats the runs for each q-head of the group.
 struct QRuns {
   int32_t seg, j, split, nP, has_prompt, seq_lo, num_runs, per_head, group, hk;
-  int32_t k0, k_end;  // key rows of the item
+  int32_t k0, k_end;     // key rows of the item
+  int32_t prompt_item;   // 1 for a prompt key tile
+  int32_t acc0;          // prompt key tile: accumulator row of its first key
 
-  __device__ __forceinline__ int32_t seq_tiles(const Sched& s, int i) const {
-    return (s.off[i + 1] - s.off[i] + kTile - 1) / kTile;
-  }
   __device__ __forceinline__ void init(const Sched& s, uint32_t item, int32_t kvh) {
     seg = static_cast<int32_t>(item_seg(item));
     j = static_cast<int32_t>(item_tile(item));
     split = static_cast<int32_t>(item_split(item));
-    nP = (s.P + kTile - 1) / kTile;
     group = s.group;
     hk = kvh;
     per_head = 0;
-    if (seg == 0) {
+    k0 = s.off[seg] + j * kTile;
+    k_end = s.off[seg + 1];
+    prompt_item = s.prompt_of(seg) == seg ? 1 : 0;
+    if (prompt_item) {
+      // the group's responses are the segments right after its prompt
+      const int32_t ng = s.responses_of(seg);
+      nP = s.seg_tiles(seg);
       has_prompt = split == 0 ? 1 : 0;
-      seq_lo = (split * s.N) / s.num_splits;
-      const int seq_hi = ((split + 1) * s.N) / s.num_splits;
+      seq_lo = seg + 1 + (split * ng) / s.num_splits;
+      const int seq_hi = seg + 1 + ((split + 1) * ng) / s.num_splits;
       num_runs = has_prompt + (seq_hi - seq_lo);
       if (has_prompt) per_head += nP - j;
-      for (int i = seq_lo; i < seq_hi; ++i) per_head += seq_tiles(s, i);
-      k0 = j * kTile;
-      k_end = s.P;
+      for (int i = seq_lo; i < seq_hi; ++i) per_head += s.seg_tiles(i);
+      acc0 = s.acc_row[seg] + j * kTile;
     } else {
+      nP = 0;
       has_prompt = 0;
-      seq_lo = seg - 1;
+      seq_lo = seg;
       num_runs = 1;
-      per_head = seq_tiles(s, seg - 1) - j;
-      k0 = s.off[seg - 1] + j * kTile;
-      k_end = s.off[seg];
+      per_head = s.seg_tiles(seg) - j;
+      acc0 = 0;
     }
   }
 };
@@ -110,19 +113,19 @@ struct QIter {
   bool diag_first;
 
   __device__ __forceinline__ void load_run(const Sched& s, const QRuns& R) {
-    if (R.seg == 0 && R.has_prompt && r == 0) {
-      q_first = 0;
+    if (R.has_prompt && r == 0) {
+      q_first = s.off[R.seg];
       t_begin = R.j;
       t_end = R.nP;
-      seg_end = s.P;
+      seg_end = s.off[R.seg + 1];
       diag_first = true;
     } else {
       const int i = R.seq_lo + r - R.has_prompt;
       q_first = s.off[i];
-      t_begin = (R.seg == 0) ? 0 : R.j;
-      t_end = (s.off[i + 1] - s.off[i] + kTile - 1) / kTile;
+      t_begin = R.prompt_item ? 0 : R.j;
+      t_end = s.seg_tiles(i);
       seg_end = s.off[i + 1];
-      diag_first = R.seg != 0;
+      diag_first = !R.prompt_item;
     }
     t = t_begin;
   }
@@ -406,14 +409,15 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- epilogue
     const int k = R.k0 + row;
     const bool valid = k < R.k_end;
-    const bool prompt_item = R.seg == 0;
+    const bool prompt_item = R.prompt_item != 0;
     if (ok) ok = mbar_wait(&bar[kAccDone], 0, err, 904);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) tc_fence_after();
     if (prompt_item) {
-      // fp32 partial of this CTA's sequences for prompt key row k
-      const size_t base = (static_cast<size_t>(k) * s.Hkv + hk) * D;
-      const size_t slice = static_cast<size_t>(s.P) * s.Hkv * D;
+      // fp32 partial of this CTA's sequences for prompt key row k, at
+      // accumulator row acc0 + row (prompt rows of all groups, packed)
+      const size_t base = (static_cast<size_t>(R.acc0 + row) * s.Hkv + hk) * D;
+      const size_t slice = static_cast<size_t>(s.acc_rows) * s.Hkv * D;
       float* pk_out = acc_k + (deterministic ? R.split * slice : 0) + base;
       float* pv_out = acc_v + (deterministic ? R.split * slice : 0) + base;
 #pragma unroll

@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) p[i] = (cb + i > row) ? 0.f : p[i];
       } else if (mk == 2) {
-        const int lim = w.P - w.k0(j) - cb;
+        const int lim = w.key_limit(j) - cb;
 #pragma unroll
         for (int i = 0; i < 64; ++i) p[i] = (i >= lim) ? 0.f : p[i];
       }

@@ -88,11 +88,15 @@ __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
   return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 }
 
-// P = exp2(c*S - m_sub) as bf16 written over the first 64 columns of S;
-// returns the row sum of the (unrounded) probabilities.
+// P = exp2(c*S - m_sub) as bf16 written over the first 64 columns of S.
+// Returns the row sums of the probabilities before (.x) and after (.y)
+// rounding to bf16: PV multiplies the rounded values, so O is normalised by
+// their sum (the weights then add up to one), while the LSE keeps the exact
+// sum.
 template <bool MASKED>
-__device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c, float m_sub) {
+__device__ __forceinline__ float2 row_exp(uint32_t tS, int lim, float c, float m_sub) {
   float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float rr_lo = 0.f, rr_hi = 0.f;
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_sub, -m_sub);
 #pragma unroll
   for (int hc = 0; hc < 2; ++hc) {
@@ -112,11 +116,12 @@ __device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c, float m_
       }
       rs[i & 3] = add2(rs[i & 3], e);
       p[i] = pack_bf16x2(e.x, e.y);
+      add_bf16x2_f32(rr_lo, rr_hi, p[i]);
     }
     tmem_st32(tS + hc * 32, p);
   }
   const float2 t = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
-  return t.x + t.y;
+  return make_float2(t.x + t.y, rr_lo + rr_hi);
 }
 
 template <int D>
@@ -260,13 +265,14 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tO = tmem + lane_off + col_o(x);
     const float c = s.scale_log2;
     float m_use = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;   // sum of the fp32 probabilities (for the LSE)
+    float lr = 0.f;  // sum of their bf16 roundings (normalises O)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(&bar[kSFull + x], j & 1, err, 301)) { ok = false; break; }
       tc_fence_after();
       const int mk = w.mask_kind(j);
-      const int lim = (mk == 2) ? (w.P - w.k0(j)) : (mk == 1 ? row + 1 : kTile);  // columns >= lim are masked
+      const int lim = (mk == 2) ? w.key_limit(j) : (mk == 1 ? row + 1 : kTile);  // columns >= lim are masked
       const float mt = (mk == 0) ? row_max<false>(tS, lim) : row_max<true>(tS, lim);
       const float m_cand = mt * c;
       // Keep the running maximum unless it grows by more than 2^8: the final
@@ -288,8 +294,9 @@ __global__ void __launch_bounds__(320, 1)
           tmem_st32(tO + ci * 32, r);
         }
       }
-      const float rs = (mk == 0) ? row_exp<false>(tS, lim, c, m_sub) : row_exp<true>(tS, lim, c, m_sub);
-      l = l * alpha + rs;
+      const float2 rs = (mk == 0) ? row_exp<false>(tS, lim, c, m_sub) : row_exp<true>(tS, lim, c, m_sub);
+      l = l * alpha + rs.x;
+      lr = lr * alpha + rs.y;
       m_use = m_new;
       tmem_st_wait();
       tc_fence_before();
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int q = w.q0 + row;
       const bool valid = q < w.q_end;
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(q) * s.Hq + h) * D);
 #pragma unroll
       for (int ci = 0; ci < D / 32; ++ci) {

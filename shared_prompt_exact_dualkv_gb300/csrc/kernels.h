@@ -32,9 +32,18 @@ cudaError_t launch_dkdv(const Sched& s, int d, const CUtensorMap& mQ, const CUte
                         void* dk, void* dv, float* acc_k, float* acc_v, int deterministic,
                         unsigned int* err, cudaStream_t stream);
 
+// Where each group's prompt rows sit: accumulator rows [acc_row[g],
+// acc_row[g+1]) hold the prompt that starts at packed row packed_row[g].
+struct PromptMap {
+  int32_t ngroups;
+  int32_t acc_row[kMaxSeg + 1];
+  int32_t packed_row[kMaxSeg];
+};
+
 // Prompt rows of dK/dV: sum the `nsplit` fp32 slices (stride `slice` floats)
-// in split order and round to bf16 (RNE) into dk/dv rows [0, P).
+// of the accumulator in split order and round to bf16 (RNE) into the
+// prompt rows of dk/dv (row_elems = Hkv * d values per row).
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
-                                 void* dk, void* dv, size_t n, cudaStream_t stream);
+                                 void* dk, void* dv, const PromptMap& map, int row_elems, cudaStream_t stream);
 
 }  // namespace dkv

@@ -348,4 +348,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// a += low bf16 half of p, b += high half, each converted exactly to fp32
+// and added with round-to-nearest (mixed-precision add of sm_100 and later).
+__device__ __forceinline__ void add_bf16x2_f32(float& a, float& b, uint32_t p) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(p));
+}
+
 }  // namespace dkv

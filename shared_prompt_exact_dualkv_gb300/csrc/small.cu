@@ -46,12 +46,23 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   for (int64_t i = tid; i < zero_n4; i += nthreads) zero_ptr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-__global__ void __launch_bounds__(256) prompt_reduce_kernel(const float4* __restrict__ src_k, const float4* __restrict__ src_v,
-                                                            int nsplit, int64_t slice4, uint2* __restrict__ dk,
-                                                            uint2* __restrict__ dv, int64_t n4) {
+__global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constant__ PromptMap map,
+                                                            const float4* __restrict__ src_k,
+                                                            const float4* __restrict__ src_v, int nsplit,
+                                                            int64_t slice4, uint2* __restrict__ dk,
+                                                            uint2* __restrict__ dv, int row4) {
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+  const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
   for (int64_t i = tid; i < n4; i += nthreads) {
+    const int32_t r = static_cast<int32_t>(i / row4);
+    // group of accumulator row r: last g with acc_row[g] <= r
+    int lo = 0, hi = map.ngroups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (map.acc_row[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int64_t out = (int64_t(map.packed_row[lo]) + (r - map.acc_row[lo])) * row4 + (i - int64_t(r) * row4);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const float4* src = which ? src_v : src_k;
@@ -63,12 +74,12 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const float4* __rest
         a.z += b.z;
         a.w += b.w;
       }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(a.x, a.y);
+      __nv_bfloat162 hi2 = __floats2bfloat162_rn(a.z, a.w);
       uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      (which ? dv : dk)[i] = pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+      (which ? dv : dk)[out] = pk;
     }
   }
 }
@@ -102,12 +113,14 @@ cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, in
 }
 
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice, void* dk,
-                                 void* dv, size_t n, cudaStream_t stream) {
-  const int64_t n4 = static_cast<int64_t>(n / 4);
+                                 void* dv, const PromptMap& map, int row_elems, cudaStream_t stream) {
+  if (map.ngroups == 0) return cudaSuccess;
+  const int row4 = row_elems / 4;
+  const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
   if (n4 == 0) return cudaSuccess;
   prompt_reduce_kernel<<<grid_for(n4), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(src_k), reinterpret_cast<const float4*>(src_v), nsplit,
-      static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv), n4);
+      map, reinterpret_cast<const float4*>(src_k), reinterpret_cast<const float4*>(src_v), nsplit,
+      static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv), row4);
   return cudaGetLastError();
 }
 

@@ -25,7 +25,8 @@ DUALKV_ERR_TIMEOUT = 6
 
 EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
             "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
-            "dualkv_bwd_static_workspace")
+            "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
+            "dualkv_bwd_groups")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -58,6 +59,16 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_bwd_static_workspace.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32,
                                                  c_i32, c_f, ctypes.c_int, c_i32, c_p, c_p, c_p, c_p]
     lib.dualkv_bwd_static_workspace.restype = ctypes.c_int
+    p_i64 = ctypes.POINTER(ctypes.c_int64)
+    lib.dualkv_fwd_groups.argtypes = [c_p, c_p, c_p, c_i32, p_i64, p_i32, p_i32, c_i32, c_i32, c_i32, c_f, c_p,
+                                      c_p, c_p]
+    lib.dualkv_fwd_groups.restype = ctypes.c_int
+    lib.dualkv_bwd_groups_workspace_bytes.argtypes = [c_i32, p_i64, p_i32, p_i32, c_i32, c_i32, c_i32, ctypes.c_int,
+                                                      c_i32]
+    lib.dualkv_bwd_groups_workspace_bytes.restype = ctypes.c_size_t
+    lib.dualkv_bwd_groups.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, p_i64, p_i32, p_i32, c_i32, c_i32,
+                                      c_i32, c_f, ctypes.c_int, c_i32, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p]
+    lib.dualkv_bwd_groups.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -149,6 +160,50 @@ def dualkv_bwd_static_workspace(q, k, v, out, dout, lse, P: int, R_lens: Sequenc
     return st
 
 
+def _groups(groups):
+    """[(P_g, [R_g,0, ...]), ...] -> (G, P array, N array, concatenated R array)."""
+    G = len(groups)
+    Ps = (ctypes.c_int64 * max(G, 1))(*[int(p) for p, _ in groups])
+    Ns = (ctypes.c_int32 * max(G, 1))(*[len(r) for _, r in groups])
+    flat = [int(x) for _, r in groups for x in r]
+    Rs = (ctypes.c_int32 * max(len(flat), 1))(*flat)
+    return G, Ps, Ns, Rs
+
+
+def dualkv_fwd_groups(q, k, v, groups, out, lse, softmax_scale: float, stream=None, check: bool = True) -> int:
+    """Calls dualkv_fwd_groups; `groups` lists (prompt length, response lengths) per group in row order."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G, Ps, Ns, Rs = _groups(groups)
+    st = lib.dualkv_fwd_groups(_ptr(q), _ptr(k), _ptr(v), G, Ps, Ns, Rs, Hq, Hkv, d, float(softmax_scale),
+                               _ptr(out), _ptr(lse), _stream(stream))
+    if check:
+        _check(st, "dualkv_fwd_groups")
+    return st
+
+
+def dualkv_bwd_groups_workspace_bytes(groups, Hq: int, Hkv: int, d: int, deterministic: bool,
+                                      num_splits: int = 0) -> int:
+    G, Ps, Ns, Rs = _groups(groups)
+    return int(lib.dualkv_bwd_groups_workspace_bytes(G, Ps, Ns, Rs, int(Hq), int(Hkv), int(d),
+                                                     1 if deterministic else 0, int(num_splits)))
+
+
+def dualkv_bwd_groups(q, k, v, out, dout, lse, groups, softmax_scale: float, deterministic: bool, workspace,
+                      dq, dk, dv, num_splits: int = 0, stream=None, check: bool = True) -> int:
+    """Calls dualkv_bwd_groups (argument meaning as dualkv_bwd, layout as dualkv_fwd_groups)."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G, Ps, Ns, Rs = _groups(groups)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.dualkv_bwd_groups(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), G, Ps, Ns, Rs, Hq,
+                               Hkv, d, float(softmax_scale), 1 if deterministic else 0, int(num_splits),
+                               _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
+    if check:
+        _check(st, "dualkv_bwd_groups")
+    return st
+
+
 def dualkv_last_device_error(stream=None):
     """Synchronises the stream and returns (status, site) of the device error word."""
     site = ctypes.c_int32(0)
@@ -201,4 +256,33 @@ def backward(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_sca
     dv = torch.empty_like(v)
     dualkv_bwd(q, k, v, out, dout, lse, P, R_lens, softmax_scale, deterministic, workspace, dq, dk, dv,
                num_splits=num_splits, stream=stream)
+    return dq, dk, dv
+
+
+def forward_groups(q, k, v, groups, softmax_scale: Optional[float] = None, stream=None):
+    """Allocates out/lse and runs dualkv_fwd_groups; returns (out, lse)."""
+    T, Hq, d = q.shape
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    dualkv_fwd_groups(q, k, v, groups, out, lse, softmax_scale, stream)
+    return out, lse
+
+
+def backward_groups(q, k, v, out, dout, lse, groups, softmax_scale: Optional[float] = None,
+                    deterministic: bool = False, num_splits: int = 0, stream=None, workspace=None):
+    """Allocates dq/dk/dv (and the workspace unless given) and runs dualkv_bwd_groups."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    if workspace is None:
+        nbytes = dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, deterministic, num_splits)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dualkv_bwd_groups(q, k, v, out, dout, lse, groups, softmax_scale, deterministic, workspace, dq, dk, dv,
+                      num_splits=num_splits, stream=stream)
     return dq, dk, dv

@@ -122,14 +122,28 @@ class Inputs:
     dout: torch.Tensor
 
 
-def make_inputs(w: Workload, seed: int = 0) -> Inputs:
+def draw_inputs(T: int, Hq: int, Hkv: int, d: int, seed: int = 0) -> Inputs:
+    """q, k, v, dout of T packed rows, drawn in that order from one seeded stream."""
     g = torch.Generator("cpu").manual_seed(seed)
-    T = w.T
-    q = torch.randn((T, w.Hq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    k = torch.randn((T, w.Hkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn((T, w.Hkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    dout = torch.randn((T, w.Hq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn((T, Hq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((T, Hkv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dout = torch.randn((T, Hq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
     return Inputs(q, k, v, dout)
+
+
+def make_inputs(w: Workload, seed: int = 0) -> Inputs:
+    return draw_inputs(w.T, w.Hq, w.Hkv, w.d, seed)
+
+
+def group_rows(groups) -> int:
+    """Packed rows of several prompt groups [(P_g, R_lens_g), ...]."""
+    return int(sum(int(p) + sum(int(r) for r in rs) for p, rs in groups))
+
+
+def make_group_inputs(groups, Hq: int, Hkv: int, d: int, seed: int = 0) -> Inputs:
+    """Inputs of a batch of several prompt groups laid out one after another."""
+    return draw_inputs(group_rows(groups), Hq, Hkv, d, seed)
 
 
 def to_f64(x: torch.Tensor) -> np.ndarray:

@@ -80,8 +80,9 @@ def test_fwd_argument_errors(D):
     assert fwd(D, k=A + 8) == D.DUALKV_ERR_ALIGNMENT
     assert fwd(D, out=A + 2) == D.DUALKV_ERR_ALIGNMENT
     assert fwd(D, scale=float("nan")) == D.DUALKV_ERR_INVALID_ARG
-    # more 128-row tiles than one launch schedules
-    assert fwd(D, P=0, N=1, R=_lens(128 * 6000)) == D.DUALKV_ERR_UNSUPPORTED
+    # a prompt or response of more than 65535 tiles of 128 rows
+    assert fwd(D, P=0, N=1, R=_lens(128 * 65535 + 1)) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd(D, P=128 * 65535 + 1) == D.DUALKV_ERR_UNSUPPORTED
     # empty input is a no-op, whatever the pointers
     assert fwd(D, P=0, N=2, R=_lens(0, 0), q=None, out=None) == D.DUALKV_OK
 
@@ -120,3 +121,59 @@ def test_trace_api_on_cpu(D):
     assert all(v == (0.0, 0) for v in D.dualkv_trace_read().values())
     D.dualkv_trace_enable(False)
     assert D.lib.dualkv_trace_read(None, None, 5) == D.DUALKV_ERR_INVALID_ARG
+
+
+def _grp(D, groups):
+    return D._groups(groups)
+
+
+def fwd_groups(D, groups=((128, (64, 64)), (0, (5,))), G=None, P=None, N=None, R=None, **kw):
+    g, Ps, Ns, Rs = _grp(D, groups)
+    args = dict(q=A, k=A, v=A, Hq=2, Hkv=1, d=64, scale=0.125, out=A, lse=A)
+    args.update(kw)
+    return D.lib.dualkv_fwd_groups(args["q"], args["k"], args["v"], g if G is None else G, Ps if P is None else P,
+                                   Ns if N is None else N, Rs if R is None else R, args["Hq"], args["Hkv"],
+                                   args["d"], args["scale"], args["out"], args["lse"], None)
+
+
+def test_fwd_groups_argument_errors(D):
+    assert fwd_groups(D, G=0) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, groups=((-1, (4,)),)) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, groups=((4, (4, -2)),)) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, N=(ctypes.c_int32 * 2)(2, -1)) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, P=ctypes.cast(None, ctypes.POINTER(ctypes.c_int64))) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, R=ctypes.cast(None, ctypes.POINTER(ctypes.c_int32))) == D.DUALKV_ERR_INVALID_ARG
+    # at most 1040 segments (groups + responses) per call
+    ws = D.dualkv_bwd_groups_workspace_bytes
+    assert ws([(1, (1,) * 519), (1, (1,) * 519)], 2, 1, 64, False, 0) > 0
+    assert ws([(1, (1,) * 519), (1, (1,) * 520)], 2, 1, 64, False, 0) == 0
+    assert ws([(1, (1,) * 1039)], 2, 1, 64, False, 0) > 0
+    assert fwd_groups(D, groups=[(1, (1,) * 1040)]) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_groups(D, d=96) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd_groups(D, groups=((128 * 65535 + 1, ()),)) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd_groups(D, out=A + 2) == D.DUALKV_ERR_ALIGNMENT
+    # groups without responses need no R array; all-empty groups are a no-op
+    assert fwd_groups(D, groups=((0, ()), (0, (0, 0))), q=None) == D.DUALKV_OK
+    assert fwd_groups(D, groups=((0, ()),), R=ctypes.cast(None, ctypes.POINTER(ctypes.c_int32)),
+                      q=None) == D.DUALKV_OK
+
+
+@pytest.mark.parametrize("groups,Hq,Hkv,d", [(((128, (64, 64)), (0, (5,)), (300, ())), 2, 1, 64),
+                                             (((33, (7,)), (0, (9, 9)), (100, (1, 2, 3))), 4, 2, 128)])
+def test_groups_workspace_bytes(D, groups, Hq, Hkv, d):
+    T = sum(p + sum(r) for p, r in groups)
+    slice_ = sum(p for p, _ in groups) * Hkv * d * 4
+    atomic = D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, False, 0)
+    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    maxN = max(len(r) for _, r in groups)
+    for S in (1, 2, 3):
+        det = D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, True, S)
+        assert det == _align256(T * Hq * 4) + 2 * _align256(max(1, min(S, maxN)) * slice_)
+
+
+@pytest.mark.parametrize("P,R,Hq,Hkv,d", [(128, (64, 64, 64, 64), 2, 1, 64), (300, (200, 0, 131), 4, 2, 128)])
+def test_one_group_workspace_matches_single_prompt_call(D, P, R, Hq, Hkv, d):
+    for det in (False, True):
+        for S in (0, 1, 2):
+            assert (D.dualkv_bwd_groups_workspace_bytes([(P, R)], Hq, Hkv, d, det, S) ==
+                    D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, det, S))

@@ -358,3 +358,95 @@ def test_planted_prompt_grads_not_summed(monkeypatch):
     monkeypatch.setattr(ora, "dualkv_backward", first_only)
     with pytest.raises(AssertionError):
         test_finite_differences()
+
+
+# --------------------------------------------------------------------------- several prompt groups
+
+def group_mask(groups):
+    """Dense [T, T] visibility of the packed multi-group batch, written from
+    the rule alone: key j is visible to row t iff both are in the same group
+    and j <= t, except that a response row sees only its own response's keys
+    besides the group's prompt."""
+    seg = []        # per row: (group, response index or -1 for the prompt)
+    for gi, (P_g, R_g) in enumerate(groups):
+        seg += [(gi, -1)] * P_g
+        for i, r in enumerate(R_g):
+            seg += [(gi, i)] * r
+    T = len(seg)
+    m = np.zeros((T, T), dtype=bool)
+    for t in range(T):
+        for j in range(t + 1):
+            same_group = seg[j][0] == seg[t][0]
+            m[t, j] = same_group and (seg[j][1] == -1 or seg[j][1] == seg[t][1])
+    return m
+
+
+def sdpa_dense(q, k, v, do, mask, scale):
+    """fp64 torch SDPA with autograd over the packed rows under a dense mask:
+    every packed row appears once, so autograd gives the packed gradient."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    g = Hq // Hkv
+    qt, kt, vt = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    qh = qt.permute(1, 0, 2)
+    kh = kt.repeat_interleave(g, dim=1).permute(1, 0, 2)
+    vh = vt.repeat_interleave(g, dim=1).permute(1, 0, 2)
+    mt = torch.tensor(mask)
+    o = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mt, scale=scale)
+    s = (scale * qh @ kh.transpose(-1, -2)).masked_fill(~mt, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    (o * torch.tensor(do).permute(1, 0, 2)).sum().backward()
+    return (o.detach().permute(1, 0, 2).numpy(), lse.detach().numpy(), qt.grad.numpy(), kt.grad.numpy(),
+            vt.grad.numpy())
+
+
+GROUP_CASES = [
+    [(5, [3, 0, 4]), (0, [2, 6]), (7, [1]), (4, [])],     # ragged; P_g = 0; N_g = 1; N_g = 0
+    [(9, [2, 2]), (9, [2, 2])],                           # two equal groups
+    [(3, [4])],                                           # one group
+]
+
+
+@pytest.mark.parametrize("groups", GROUP_CASES)
+def test_groups_against_dense_mask_sdpa(groups):
+    T = ora.group_row_starts(groups)[-1]
+    Hq, Hkv, d = 4, 2, 8
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((T, Hq, d))
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    do = rng.standard_normal((T, Hq, d))
+    scale = 1 / math.sqrt(d)
+    out, lse = ora.dualkv_forward_groups(q, k, v, groups, scale)
+    dq, dk, dv = ora.dualkv_backward_groups(q, k, v, do, groups, scale)
+    to, tl, tdq, tdk, tdv = sdpa_dense(q, k, v, do, group_mask(groups), scale)
+    np.testing.assert_allclose(out, to, atol=1e-12)
+    np.testing.assert_allclose(lse, tl, atol=1e-12)
+    np.testing.assert_allclose(dq, tdq, atol=1e-11)
+    np.testing.assert_allclose(dk, tdk, atol=1e-11)
+    np.testing.assert_allclose(dv, tdv, atol=1e-11)
+
+
+def test_group_mask_single_group_matches_replicated_sdpa():
+    """The dense-mask formulation agrees with the replicated-sequence one on a
+    single group (ties the two library cross-checks together)."""
+    P, R_lens, Hq, Hkv, d = 6, [3, 0, 5], 2, 1, 4
+    q, k, v, do = rand_case(P, R_lens, Hq, Hkv, d, seed=12)
+    a = sdpa_dense(q, k, v, do, group_mask([(P, R_lens)]), 0.5)
+    b = sdpa_packed(q, k, v, do, P, R_lens, 0.5)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+
+
+def test_planted_group_leak_is_caught(monkeypatch):
+    """A group oracle that shifts the groups' row ranges by one row fails the
+    dense-mask pin."""
+    real = ora.group_row_starts
+
+    def shifted(groups):
+        s = list(real(groups))
+        s[1] += 1
+        return s
+
+    monkeypatch.setattr(ora, "group_row_starts", shifted)
+    with pytest.raises((AssertionError, ValueError)):
+        test_groups_against_dense_mask_sdpa(GROUP_CASES[0])
