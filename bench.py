@@ -36,6 +36,10 @@ METRIC = "DualKV fwd+bwd ms and useful TFLOP/s (% of GB300 bf16 peak) per attn l
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def align256(x: int) -> int:
+    return (x + 255) // 256 * 256
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -164,6 +168,68 @@ def recorded_traffic(kernel: str, workload: str, deterministic: bool):
     return int(m_bytes.group(1)) if h.hexdigest() == m_hash.group(1) else None
 
 
+def end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world):
+    """Same step through the C ABI with host buffers: every step copies its
+    inputs from pinned host memory and its results (out, lse, dq, dk, dv) back.
+    Two device buffer sets let step k+1's host-to-device copies (copy-in
+    stream) and step k-1's device-to-host copies (copy-out stream) overlap
+    step k's kernels.  Returns (ms per step, h2d bytes, d2h bytes)."""
+    hin = [t.pin_memory() for t in (x.q, x.k, x.v, x.dout)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    bufs = []
+    for b in range(2):
+        ins = [torch.empty_like(t, device=dev) for t in (x.q, x.k, x.v, x.dout)]
+        outs = [torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
+                torch.empty_like(v)]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        bws = torch.empty_like(ws)
+        bufs.append((ins, outs, hout, bws))
+    d2h = sum(t.numel() * t.element_size() for t in bufs[0][2])
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in_ready", "comp_done", "out_done")}
+
+    def e2e_step(i):
+        b = i & 1
+        ins, outs, hout, bws = bufs[b]
+        (eq, ek, ev_, edo), (eo, el, edq, edk, edv) = ins, outs
+        with torch.cuda.stream(cin):
+            if i >= 2:
+                cin.wait_event(ev["comp_done"][b])   # step i-2 finished reading this input set
+            for dst, src in zip(ins, hin):
+                dst.copy_(src, non_blocking=True)
+            ev["in_ready"][b].record(cin)
+        stream.wait_event(ev["in_ready"][b])
+        if i >= 2:
+            stream.wait_event(ev["out_done"][b])     # step i-2's results have left this output set
+        D.dualkv_fwd(eq, ek, ev_, w.P, w.R_lens, eo, el, w.scale, stream)
+        D.dualkv_bwd(eq, ek, ev_, eo, edo, el, w.P, w.R_lens, w.scale, det, bws, edq, edk, edv, stream=stream)
+        ev["comp_done"][b].record(stream)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev["comp_done"][b])
+            for dst, src in zip(hout, outs):
+                dst.copy_(src, non_blocking=True)
+            ev["out_done"][b].record(cout)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cin)
+    for i in range(args.steps):
+        e2e_step(i)
+    cout.wait_stream(stream)
+    cout.wait_stream(cin)
+    e1.record(cout)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    del bufs
+
+    return e2e_ms, h2d, d2h
+
+
 # --------------------------------------------------------------------------- CPU oracle timings
 
 def _oracle_seq0_inputs(w: synthetic.Workload, seed: int):
@@ -247,6 +313,8 @@ def main():
     ap.add_argument("--workload", default="p32k", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--deterministic", action="store_true", help="time the deterministic dK/dV mode")
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="also skip the end-to-end leg (for profiling: one buffer set on the device)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -303,67 +371,17 @@ def main():
     per_kernel = {name: (tot / cnt if cnt else 0.0) for name, (tot, cnt) in tr.items()}
     launches_per_step = sum(cnt for _, cnt in tr.values()) // args.steps
 
-    # End to end through the same C ABI calls with host buffers: every step
-    # copies its inputs from pinned host memory and its results (out, lse, dq,
-    # dk, dv) back.  Two device buffer sets are used so that step k+1's
-    # host-to-device copies (copy-in stream) and step k-1's device-to-host
-    # copies (copy-out stream) overlap step k's kernels.
-    hin = [t.pin_memory() for t in (x.q, x.k, x.v, x.dout)]
-    h2d = sum(t.numel() * t.element_size() for t in hin)
-    bufs = []
-    for b in range(2):
-        ins = [torch.empty_like(t, device=dev) for t in (x.q, x.k, x.v, x.dout)]
-        outs = [torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
-                torch.empty_like(v)]
-        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        bws = torch.empty_like(ws)
-        bufs.append((ins, outs, hout, bws))
-    d2h = sum(t.numel() * t.element_size() for t in bufs[0][2])
-    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in_ready", "comp_done", "out_done")}
-
-    def e2e_step(i):
-        b = i & 1
-        ins, outs, hout, bws = bufs[b]
-        (eq, ek, ev_, edo), (eo, el, edq, edk, edv) = ins, outs
-        with torch.cuda.stream(cin):
-            if i >= 2:
-                cin.wait_event(ev["comp_done"][b])   # step i-2 finished reading this input set
-            for dst, src in zip(ins, hin):
-                dst.copy_(src, non_blocking=True)
-            ev["in_ready"][b].record(cin)
-        stream.wait_event(ev["in_ready"][b])
-        if i >= 2:
-            stream.wait_event(ev["out_done"][b])     # step i-2's results have left this output set
-        D.dualkv_fwd(eq, ek, ev_, w.P, w.R_lens, eo, el, w.scale, stream)
-        D.dualkv_bwd(eq, ek, ev_, eo, edo, el, w.P, w.R_lens, w.scale, det, bws, edq, edk, edv, stream=stream)
-        ev["comp_done"][b].record(stream)
-        with torch.cuda.stream(cout):
-            cout.wait_event(ev["comp_done"][b])
-            for dst, src in zip(hout, outs):
-                dst.copy_(src, non_blocking=True)
-            ev["out_done"][b].record(cout)
-
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(cin)
-    for i in range(args.steps):
-        e2e_step(i)
-    cout.wait_stream(stream)
-    cout.wait_stream(cin)
-    e1.record(cout)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    del bufs
+    e2e = None
+    if not args.kernels_only:
+        e2e = end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world)
 
     flops = w.useful_flops()
     value = weak_scaling_value(flops, ms, world)
-    e2e_value = weak_scaling_value(flops, e2e_ms, world)
+    e2e_obj = None
+    if e2e is not None:
+        e2e_ms, h2d, d2h = e2e
+        e2e_obj = {"value": weak_scaling_value(flops, e2e_ms, world), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
@@ -376,6 +394,27 @@ def main():
                 "traffic": recorded_traffic("dkdv_kernel", w.name, det),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
                 "algorithmic": "8*d flops per unmasked (query,key) pair per q-head"}
+
+    # the two bandwidth-bound kernels of the backward, against the measured copy bandwidth
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    prompt_rows_bytes = w.P * w.Hkv * w.d * 4                      # one fp32 [P, Hkv, d] slice
+    n_slices = 1
+    if det and prompt_rows_bytes:
+        acc_region = (ws.numel() - align256(w.T * w.Hq * 4)) // 2   # bytes of acc_k (= acc_v)
+        n_slices = max(1, acc_region // prompt_rows_bytes)
+    hbm_bytes = {
+        # read O and dO, write D; zero the two fp32 accumulators in the atomic mode
+        "bwd_preprocess": 2 * w.T * w.Hq * w.d * 2 + w.T * w.Hq * 4 + (0 if det else 2 * prompt_rows_bytes),
+        # read every split slice of both accumulators, write bf16 prompt dK and dV
+        "bwd_prompt_reduce": 2 * n_slices * prompt_rows_bytes + 2 * w.P * w.Hkv * w.d * 2,
+    }
+    hbm_kernels = {}
+    for name, nbytes in hbm_bytes.items():
+        kms = per_kernel.get(name, 0.0)
+        gbs = nbytes / (kms * 1e-3) / 1e9 if kms else None
+        hbm_kernels[name] = {"bytes_per_launch": nbytes, "ms": kms, "achieved_gbs": gbs, "peak_gbs": hbm_peak,
+                             "frac": (gbs / hbm_peak) if gbs else None,
+                             "peak_source": f"{peak_src} hbm_gbs"}
 
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -392,9 +431,9 @@ def main():
         "per_kernel_ms": per_kernel,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock_info,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e_obj,
         "roofline": roofline,
+        "hbm_kernels": hbm_kernels,
     }
 
     if rank == 0 and not args.quick:
