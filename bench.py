@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -230,6 +231,80 @@ def end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world):
     return e2e_ms, h2d, d2h
 
 
+def layer_flops(shape: dict, rows: int, pairs_per_head: int) -> dict:
+    """Useful flops of one decoder layer, forward + backward: the GEMMs (2 per
+    multiply-add, three times over for forward, dX and dW) and the attention
+    (14*d per unmasked pair per q-head)."""
+    H, I = shape["hidden"], shape["inter"]
+    nq, nk = shape["Hq"] * shape["d"], shape["Hkv"] * shape["d"]
+    gemm = 3 * 2 * rows * (H * (nq + 2 * nk) + nq * H + H * 2 * I + I * H)
+    att = 14 * shape["d"] * shape["Hq"] * pairs_per_head
+    return {"gemm": float(gemm), "attention": float(att)}
+
+
+def layer_leg(D, w, dev, stream):
+    """One Qwen3-8B-shaped decoder layer (random weights), forward + backward
+    through dualkv_layer_fwd/bwd, on the packed rows of the workload and on its
+    replicated N(P+R) rows (every sequence its own causal group)."""
+    shape = synthetic.LAYER_SHAPES["qwen3_8b"]
+    cfg = D.layer_config(**shape)
+    out = {"shape": "qwen3_8b", **{k: shape[k] for k in ("hidden", "Hq", "Hkv", "d", "inter")}}
+    gen = torch.Generator(device=dev).manual_seed(11)
+    weights = {}
+    for n, sh in D.layer_weight_shapes(cfg).items():
+        r = torch.randn(sh, device=dev, generator=gen)
+        weights[n] = (1.0 + 0.1 * r if n.startswith("ln") else r / math.sqrt(sh[1])).to(torch.bfloat16)
+    layouts = {"packed": ([(w.P, tuple(w.R_lens))], w.T, w.pairs_per_head()),
+               "replicated": ([(w.P + int(r), ()) for r in w.R_lens], w.T_replicated,
+                              w.pairs_per_head_replicated())}
+    for name, (groups, rows, pairs) in layouts.items():
+        x = torch.randn((rows, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
+        dy = torch.randn((rows, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
+        layer = D.PackedLayer(cfg, weights, groups)
+        y = torch.empty_like(x)
+        dx = torch.empty_like(x)
+        grads = {n: torch.empty(t.shape, dtype=torch.float32, device=dev) for n, t in weights.items()}
+
+        def fwd():
+            D.dualkv_layer_fwd(cfg, weights, x, groups, y, layer.workspace, stream)
+
+        def bwd():
+            D.dualkv_layer_bwd(cfg, weights, x, dy, groups, dx, grads, layer.workspace, stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fwd()
+                bwd()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        f_ms = b_ms = 0.0
+        steps = 3
+        for i in range(steps):
+            ev[0].record(stream)
+            fwd()
+            ev[1].record(stream)
+            bwd()
+            ev[2].record(stream)
+            torch.cuda.synchronize()
+            f_ms += ev[0].elapsed_time(ev[1]) / steps
+            b_ms += ev[1].elapsed_time(ev[2]) / steps
+        st, site = D.dualkv_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error {st} at wait site {site}")
+        fl = layer_flops(shape, rows, pairs)
+        nbytes = layer.workspace.numel() + 4 * x.numel() * 2
+        out[name] = {"rows": rows, "fwd_ms": f_ms, "bwd_ms": b_ms, "ms": f_ms + b_ms,
+                     "gemm_tflop": fl["gemm"] / 1e12, "attention_tflop": fl["attention"] / 1e12,
+                     "tflops": (fl["gemm"] + fl["attention"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
+                     "device_bytes": nbytes}
+        del layer, x, dy, y, dx, grads
+        torch.cuda.empty_cache()
+    out["speedup_packed"] = out["replicated"]["ms"] / out["packed"]["ms"]
+    out["memory_reduction"] = 1.0 - out["packed"]["device_bytes"] / out["replicated"]["device_bytes"]
+    out["rho_tokens"] = w.rho_tokens()
+    return out
+
+
 # --------------------------------------------------------------------------- CPU oracle timings
 
 def _oracle_seq0_inputs(w: synthetic.Workload, seed: int):
@@ -313,6 +388,8 @@ def main():
     ap.add_argument("--workload", default="p32k", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--deterministic", action="store_true", help="time the deterministic dK/dV mode")
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
+    ap.add_argument("--layer", action="store_true",
+                    help="also time a Qwen3-8B-shaped decoder layer, packed against replicated")
     ap.add_argument("--kernels-only", action="store_true",
                     help="also skip the end-to-end leg (for profiling: one buffer set on the device)")
     args = ap.parse_args()
@@ -495,6 +572,11 @@ def main():
         st, site = D.dualkv_last_device_error(stream)
         if st != 0:
             raise RuntimeError(f"device error {st} at wait site {site}")
+
+    if rank == 0 and args.layer:
+        del q, k, v, do, out, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        result["layer"] = layer_leg(D, w, dev, stream)
 
     if rank == 0:
         print(json.dumps(result), flush=True)

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdualkv.so")
 
-SOURCES = ["api.cu", "fwd.cu", "dq.cu", "dkdv.cu", "small.cu"]
+SOURCES = ["api.cu", "fwd.cu", "dq.cu", "dkdv.cu", "small.cu", "layer_kernels.cu", "layer_api.cu"]
+LIBS = ["-lcublas"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]
@@ -53,7 +54,7 @@ def build(verbose: bool = False, extra=None) -> str:
         f.write("\n".join(logs))
     objs = [r[1] for r in results]
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, *LIBS]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")

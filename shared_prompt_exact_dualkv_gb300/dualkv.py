@@ -26,12 +26,32 @@ DUALKV_ERR_TIMEOUT = 6
 EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
             "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
-            "dualkv_bwd_groups")
+            "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
+            "dualkv_packed_positions")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
 
 TRACE_KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_prompt_reduce", "bwd_dq")
+
+
+LAYER_WEIGHTS = ("ln1", "wqkv", "wo", "ln2", "wgu", "wd")
+
+
+class LayerConfig(ctypes.Structure):
+    """dualkv_layer_config."""
+    _fields_ = [("hidden", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("rope_base", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+class LayerWeights(ctypes.Structure):
+    """dualkv_layer_weights: device pointers of the bf16 weights."""
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_WEIGHTS]
+
+
+class LayerGrads(ctypes.Structure):
+    """dualkv_layer_grads: device pointers of the fp32 weight gradients."""
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_WEIGHTS]
 
 
 def _load() -> ctypes.CDLL:
@@ -69,6 +89,17 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_bwd_groups.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, p_i64, p_i32, p_i32, c_i32, c_i32,
                                       c_i32, c_f, ctypes.c_int, c_i32, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p]
     lib.dualkv_bwd_groups.restype = ctypes.c_int
+    p_cfg = ctypes.POINTER(LayerConfig)
+    lib.dualkv_layer_workspace_bytes.argtypes = [p_cfg, c_i32, p_i64, p_i32, p_i32]
+    lib.dualkv_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.dualkv_layer_fwd.argtypes = [p_cfg, ctypes.POINTER(LayerWeights), c_p, c_i32, p_i64, p_i32, p_i32, c_p, c_p,
+                                     ctypes.c_size_t, c_p]
+    lib.dualkv_layer_fwd.restype = ctypes.c_int
+    lib.dualkv_layer_bwd.argtypes = [p_cfg, ctypes.POINTER(LayerWeights), c_p, c_p, c_i32, p_i64, p_i32, p_i32, c_p,
+                                     ctypes.POINTER(LayerGrads), c_p, ctypes.c_size_t, c_p]
+    lib.dualkv_layer_bwd.restype = ctypes.c_int
+    lib.dualkv_packed_positions.argtypes = [c_i32, p_i64, p_i32, p_i32, p_i32, c_i64]
+    lib.dualkv_packed_positions.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -286,3 +317,81 @@ def backward_groups(q, k, v, out, dout, lse, groups, softmax_scale: Optional[flo
     dualkv_bwd_groups(q, k, v, out, dout, lse, groups, softmax_scale, deterministic, workspace, dq, dk, dv,
                       num_splits=num_splits, stream=stream)
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------- packed decoder layer
+
+def layer_config(hidden: int, Hq: int, Hkv: int, d: int, inter: int, rope_base: float = 1.0e6,
+                 eps: float = 1.0e-6) -> LayerConfig:
+    return LayerConfig(int(hidden), int(Hq), int(Hkv), int(d), int(inter), float(rope_base), float(eps))
+
+
+def layer_weight_shapes(cfg: LayerConfig) -> dict:
+    """Shapes of the bf16 weights (and of the fp32 gradients)."""
+    return {"ln1": (cfg.hidden,), "wqkv": ((cfg.Hq + 2 * cfg.Hkv) * cfg.d, cfg.hidden),
+            "wo": (cfg.hidden, cfg.Hq * cfg.d), "ln2": (cfg.hidden,), "wgu": (2 * cfg.inter, cfg.hidden),
+            "wd": (cfg.hidden, cfg.inter)}
+
+
+def _weights(w: dict) -> LayerWeights:
+    return LayerWeights(*[_ptr(w[n]) for n in LAYER_WEIGHTS])
+
+
+def dualkv_layer_workspace_bytes(cfg: LayerConfig, groups) -> int:
+    G, Ps, Ns, Rs = _groups(groups)
+    return int(lib.dualkv_layer_workspace_bytes(ctypes.byref(cfg), G, Ps, Ns, Rs))
+
+
+def dualkv_layer_fwd(cfg: LayerConfig, weights: dict, x, groups, y, workspace, stream=None, check: bool = True) -> int:
+    """Calls dualkv_layer_fwd (x, y [T, hidden] bf16; weights: dict of bf16 device tensors)."""
+    G, Ps, Ns, Rs = _groups(groups)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.dualkv_layer_fwd(ctypes.byref(cfg), ctypes.byref(_weights(weights)), _ptr(x), G, Ps, Ns, Rs, _ptr(y),
+                              _ptr(workspace), nbytes, _stream(stream))
+    if check:
+        _check(st, "dualkv_layer_fwd")
+    return st
+
+
+def dualkv_layer_bwd(cfg: LayerConfig, weights: dict, x, dy, groups, dx, grads: dict, workspace, stream=None,
+                     check: bool = True) -> int:
+    """Calls dualkv_layer_bwd (grads: dict of fp32 device tensors, overwritten)."""
+    G, Ps, Ns, Rs = _groups(groups)
+    nbytes = workspace.numel() * workspace.element_size()
+    g = LayerGrads(*[_ptr(grads[n]) for n in LAYER_WEIGHTS])
+    st = lib.dualkv_layer_bwd(ctypes.byref(cfg), ctypes.byref(_weights(weights)), _ptr(x), _ptr(dy), G, Ps, Ns, Rs,
+                              _ptr(dx), ctypes.byref(g), _ptr(workspace), nbytes, _stream(stream))
+    if check:
+        _check(st, "dualkv_layer_bwd")
+    return st
+
+
+def dualkv_packed_positions(groups):
+    """Position id of every packed row (host list)."""
+    G, Ps, Ns, Rs = _groups(groups)
+    T = sum(int(p) + sum(int(r) for r in rs) for p, rs in groups)
+    out = (ctypes.c_int32 * max(T, 1))()
+    _check(lib.dualkv_packed_positions(G, Ps, Ns, Rs, out, T), "dualkv_packed_positions")
+    return list(out[:T])
+
+
+class PackedLayer:
+    """Forward/backward of one packed decoder layer through the C ABI, with
+    the workspace kept between the two calls."""
+
+    def __init__(self, cfg: LayerConfig, weights: dict, groups):
+        self.cfg, self.weights, self.groups = cfg, weights, [(int(p), tuple(int(r) for r in rs)) for p, rs in groups]
+        dev = weights["wqkv"].device
+        self.workspace = torch.empty(max(1, dualkv_layer_workspace_bytes(cfg, self.groups)), dtype=torch.uint8,
+                                     device=dev)
+
+    def forward(self, x, stream=None):
+        y = torch.empty_like(x)
+        dualkv_layer_fwd(self.cfg, self.weights, x, self.groups, y, self.workspace, stream)
+        return y
+
+    def backward(self, x, dy, stream=None):
+        dx = torch.empty_like(x)
+        grads = {n: torch.empty(t.shape, dtype=torch.float32, device=t.device) for n, t in self.weights.items()}
+        dualkv_layer_bwd(self.cfg, self.weights, x, dy, self.groups, dx, grads, self.workspace, stream)
+        return dx, grads

@@ -149,3 +149,30 @@ def make_group_inputs(groups, Hq: int, Hkv: int, d: int, seed: int = 0) -> Input
 def to_f64(x: torch.Tensor) -> np.ndarray:
     """Exact upcast of a bf16 tensor to a float64 numpy array."""
     return x.detach().to("cpu").to(torch.float64).numpy()
+
+
+# Decoder-layer shapes: Qwen3-8B (the pages' main model; research-map page,
+# "Experimental setup") and a small one the fp64 oracle finishes in seconds.
+LAYER_SHAPES = {
+    "qwen3_8b": dict(hidden=4096, Hq=32, Hkv=8, d=128, inter=12288, rope_base=1.0e6, eps=1.0e-6),
+    "small": dict(hidden=256, Hq=4, Hkv=2, d=64, inter=512, rope_base=1.0e4, eps=1.0e-6),
+}
+
+
+def make_layer_inputs(shape: dict, T: int, seed: int = 0):
+    """Random-init weights (bf16) and packed activations x, dy [T, hidden] (bf16).
+
+    Norm weights are 1 + 0.1 N(0,1); projection weights N(0,1)/sqrt(fan_in);
+    x and dy N(0,1).  Drawn in the order ln1, wqkv, wo, ln2, wgu, wd, x, dy
+    from one seeded CPU generator."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    H, I = shape["hidden"], shape["inter"]
+    nq, nk = shape["Hq"] * shape["d"], shape["Hkv"] * shape["d"]
+    shapes = {"ln1": (H,), "wqkv": (nq + 2 * nk, H), "wo": (H, nq), "ln2": (H,), "wgu": (2 * I, H), "wd": (H, I)}
+    w = {}
+    for n, sh in shapes.items():
+        r = torch.randn(sh, generator=g, dtype=torch.float32)
+        w[n] = (1.0 + 0.1 * r if n.startswith("ln") else r / math.sqrt(sh[1])).to(torch.bfloat16)
+    x = torch.randn((T, H), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dy = torch.randn((T, H), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return w, x, dy

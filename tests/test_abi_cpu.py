@@ -8,7 +8,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dualkv.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("dualkv.h", "dualkv_layer.h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,8 +21,10 @@ def D():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return re.findall(r"DUALKV_API\s+[\w\s\*]+?\b(dualkv_\w+)\s*\(", text)
+    names = []
+    for h in HEADERS:
+        names += re.findall(r"DUALKV_API\s+[\w\s\*]+?\b(dualkv_\w+)\s*\(", open(h).read())
+    return names
 
 
 def test_header_declares_expected_entry_points():
@@ -177,3 +179,39 @@ def test_one_group_workspace_matches_single_prompt_call(D, P, R, Hq, Hkv, d):
         for S in (0, 1, 2):
             assert (D.dualkv_bwd_groups_workspace_bytes([(P, R)], Hq, Hkv, d, det, S) ==
                     D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, det, S))
+
+
+# --------------------------------------------------------------------------- packed decoder layer
+
+def test_packed_positions_match_oracle(D):
+    from oracle import layer as L
+    groups = [(5, (3, 0, 4)), (0, (2, 6)), (7, ()), (2, (1,))]
+    assert D.dualkv_packed_positions(groups) == list(L.packed_positions(groups))
+
+
+def test_layer_argument_errors(D):
+    cfg = D.layer_config(256, 4, 2, 64, 512)
+    groups = [(128, (64, 64))]
+    assert D.dualkv_layer_workspace_bytes(cfg, groups) > 0
+    for bad, code in ((D.layer_config(256, 4, 2, 96, 512), 0), (D.layer_config(252, 4, 2, 64, 512), 0),
+                      (D.layer_config(256, 3, 2, 64, 512), 0), (D.layer_config(256, 4, 2, 64, 512, eps=-1.0), 0),
+                      (D.layer_config(256, 4, 2, 64, 512, rope_base=0.5), 0)):
+        assert D.dualkv_layer_workspace_bytes(bad, groups) == code
+    assert D.dualkv_layer_workspace_bytes(cfg, [(-1, (4,))]) == 0
+    G, Ps, Ns, Rs = D._groups(groups)
+    W = D.LayerWeights(*([A] * 6))
+    gr = D.LayerGrads(*([A] * 6))
+    ws = D.dualkv_layer_workspace_bytes(cfg, groups)
+    fwd = lambda **kw: D.lib.dualkv_layer_fwd(ctypes.byref(kw.get("cfg", cfg)), ctypes.byref(kw.get("W", W)),
+                                               kw.get("x", A), G, Ps, Ns, Rs, kw.get("y", A), kw.get("ws", A),
+                                               kw.get("nbytes", ws), None)
+    assert fwd(cfg=D.layer_config(256, 4, 2, 96, 512)) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd(W=D.LayerWeights(*([A] * 5 + [None]))) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(W=D.LayerWeights(*([A] * 5 + [A + 8]))) == D.DUALKV_ERR_ALIGNMENT
+    assert fwd(x=None) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd(ws=A + 16) == D.DUALKV_ERR_ALIGNMENT
+    assert fwd(nbytes=ws - 1) == D.DUALKV_ERR_WORKSPACE
+    bwd = lambda **kw: D.lib.dualkv_layer_bwd(ctypes.byref(cfg), ctypes.byref(W), A, A, G, Ps, Ns, Rs, A,
+                                               ctypes.byref(kw.get("gr", gr)), A, kw.get("nbytes", ws), None)
+    assert bwd(gr=D.LayerGrads(*([A] * 5 + [None]))) == D.DUALKV_ERR_INVALID_ARG
+    assert bwd(nbytes=16) == D.DUALKV_ERR_WORKSPACE
