@@ -112,3 +112,21 @@ def test_empty_input_is_noop():
     k = torch.empty((0, 1, 128), dtype=torch.bfloat16, device="cuda")
     out, lse = dk_.forward(q, k, k, 0, (0, 0), 0.1)
     assert out.numel() == 0 and lse.numel() == 0
+
+
+def test_reduction_modes_agree():
+    """The two reduction modes differ only in how prompt dK/dV partials are
+    summed: dQ and the response rows of dK/dV are the same bits, and the
+    prompt rows agree to fp32 summation order."""
+    dk_ = _lib()
+    w = synthetic.make_workload("modes", 4, 2, 128, 300, (200, 0, 131, 128))
+    _, (q, k, v, do) = _device_inputs(w, seed=8)
+    out, lse = dk_.forward(q, k, v, w.P, w.R_lens, w.scale)
+    a = dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=False, num_splits=3)
+    b = dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=True, num_splits=3)
+    assert torch.equal(a[0], b[0])
+    P = w.P
+    for x, y in zip(a[1:], b[1:]):
+        assert torch.equal(x[P:], y[P:])
+        diff = (x[:P].float() - y[:P].float()).norm() / y[:P].float().norm()
+        assert diff.item() <= 1e-3
