@@ -55,15 +55,17 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const uint4* 
   const int64_t nwarps = (int64_t(gridDim.x) * kNormThreads) >> 5;
   const float inv_h = 1.f / (8.f * groups);
   for (int64_t r = warp0; r < rows; r += nwarps) {
-    float v[NG][8];
+    uint4 pk[NG];  // the row stays packed (bf16) between the two passes
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < NG; ++j) {
       const int gi = lane + 32 * j;
       if (gi < groups) {
-        unpack8(x[r * groups + gi], v[j]);
+        float v[8];
+        pk[j] = x[r * groups + gi];
+        unpack8(pk[j], v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
       }
     }
     ss = warp_sum(ss);
@@ -72,10 +74,11 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const uint4* 
     for (int j = 0; j < NG; ++j) {
       const int gi = lane + 32 * j;
       if (gi < groups) {
-        float wf[8], o[8];
+        float v[8], wf[8], o[8];
+        unpack8(pk[j], v);
         unpack8(w[gi], wf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = v[j][e] * rs * wf[e];
+        for (int e = 0; e < 8; ++e) o[e] = v[e] * rs * wf[e];
         y[r * groups + gi] = pack8(o);
       }
     }
@@ -83,28 +86,20 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_fwd_kernel(const uint4* 
   }
 }
 
-// dx = dres + r*(w*dy) - (r^3/H) * x * sum(w*dy*x); each warp also adds
-// dy*x*r into its own fp32 row of dw partials in shared memory, and the
-// block writes the sum of its warps' partials to part[blockIdx.x].
+// dx = dres + r*(w*dy) - (r^3/H) * x * sum(w*dy*x), one warp per row; the
+// second pass reads the row again (from L1).
 template <int NG>
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_dx_kernel(
     const uint4* __restrict__ dy, const uint4* __restrict__ x, const uint4* __restrict__ w,
-    const float* __restrict__ rstd, const uint4* __restrict__ dres, uint4* __restrict__ dx, float* __restrict__ part,
-    int64_t rows, int groups) {
-  extern __shared__ float sdw[];  // [4][8 * groups]
+    const float* __restrict__ rstd, const uint4* __restrict__ dres, uint4* __restrict__ dx, int64_t rows,
+    int groups) {
   const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int H = 8 * groups;
-  for (int i = threadIdx.x; i < 4 * H; i += kNormThreads) sdw[i] = 0.f;
-  __syncthreads();
-  float* mine = sdw + wib * H;
   const int64_t warp0 = (int64_t(blockIdx.x) * kNormThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kNormThreads) >> 5;
-  const float inv_h = 1.f / H;
+  const float inv_h = 1.f / (8.f * groups);
   for (int64_t r = warp0; r < rows; r += nwarps) {
     float dot = 0.f;
     const float rs = rstd[r];
-    // pass 1: sum(w*dy*x) and this warp's dw partial
 #pragma unroll 4
     for (int j = 0; j < NG; ++j) {
       const int gi = lane + 32 * j;
@@ -114,15 +109,11 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(
         unpack8(x[r * groups + gi], xv);
         unpack8(w[gi], wf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          dot = fmaf(g[e] * wf[e], xv[e], dot);
-          mine[gi * 8 + e] = fmaf(g[e] * xv[e], rs, mine[gi * 8 + e]);
-        }
+        for (int e = 0; e < 8; ++e) dot = fmaf(g[e] * wf[e], xv[e], dot);
       }
     }
     dot = warp_sum(dot);
     const float c = rs * rs * rs * dot * inv_h;
-    // pass 2: the row again (from L1), dx = dres + r*w*dy - c*x
 #pragma unroll 4
     for (int j = 0; j < NG; ++j) {
       const int gi = lane + 32 * j;
@@ -138,9 +129,32 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_bwd_kernel(
       }
     }
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < H; i += kNormThreads)
-    part[int64_t(blockIdx.x) * H + i] = (sdw[i] + sdw[H + i]) + (sdw[2 * H + i] + sdw[3 * H + i]);
+}
+
+// Partial dw of a contiguous chunk of rows: thread t of the block owns the 8
+// columns of group t (and t + blockDim, ...) and sums dy*x*r over the chunk;
+// part[blockIdx.x][column] = that sum.
+__global__ void __launch_bounds__(256) rmsnorm_dw_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ x,
+                                                         const float* __restrict__ rstd, float* __restrict__ part,
+                                                         int64_t rows, int groups) {
+  const int64_t chunk = (rows + gridDim.x - 1) / gridDim.x;
+  const int64_t r0 = int64_t(blockIdx.x) * chunk;
+  const int64_t r1 = r0 + chunk < rows ? r0 + chunk : rows;
+  for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int64_t r = r0; r < r1; ++r) {
+      float g[8], xv[8];
+      unpack8(dy[r * groups + gi], g);
+      unpack8(x[r * groups + gi], xv);
+      const float rs = rstd[r];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(g[e] * xv[e], rs, acc[e]);
+    }
+    float4* dst = reinterpret_cast<float4*>(part + int64_t(blockIdx.x) * groups * 8 + gi * 8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
 }
 
 // dw[c] = sum over the blocks' partials, in block order.
@@ -303,21 +317,20 @@ cudaError_t norm_fwd_ng(const void* x, const void* w, void* y, float* rstd, int6
 }
 
 template <int NG>
-cudaError_t norm_bwd_ng(const void* dy, const void* x, const void* w, const float* rstd, const void* dres, void* dx,
-                        float* part, int nblocks, int64_t rows, int groups, cudaStream_t st) {
-  const size_t smem = size_t(4) * 8 * groups * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(rmsnorm_bwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  rmsnorm_bwd_kernel<NG><<<nblocks, kNormThreads, smem, st>>>(
+cudaError_t norm_dx_ng(const void* dy, const void* x, const void* w, const float* rstd, const void* dres, void* dx,
+                       int64_t rows, int groups, cudaStream_t st) {
+  int64_t blocks = (rows + 3) / 4;
+  const int64_t cap = int64_t(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  rmsnorm_dx_kernel<NG><<<static_cast<int>(blocks), kNormThreads, 0, st>>>(
       static_cast<const uint4*>(dy), static_cast<const uint4*>(x), static_cast<const uint4*>(w), rstd,
-      static_cast<const uint4*>(dres), static_cast<uint4*>(dx), part, rows, groups);
+      static_cast<const uint4*>(dres), static_cast<uint4*>(dx), rows, groups);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int rmsnorm_bwd_blocks() { return sm_count() * 2; }
+int rmsnorm_bwd_blocks() { return sm_count() * 4; }
 
 cudaError_t launch_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int hidden,
                                float eps, cudaStream_t st) {
@@ -336,12 +349,18 @@ cudaError_t launch_rmsnorm_bwd(const void* dy, const void* x, const void* w, con
   const int groups = hidden / 8;
   const int ng = (groups + 31) / 32;
   const int nblocks = rmsnorm_bwd_blocks();
-  cudaError_t e;
-  if (ng <= 4) e = norm_bwd_ng<4>(dy, x, w, rstd, dres, dx, part, nblocks, rows, groups, st);
-  else if (ng <= 8) e = norm_bwd_ng<8>(dy, x, w, rstd, dres, dx, part, nblocks, rows, groups, st);
-  else if (ng <= 16) e = norm_bwd_ng<16>(dy, x, w, rstd, dres, dx, part, nblocks, rows, groups, st);
-  else if (ng <= 24) e = norm_bwd_ng<24>(dy, x, w, rstd, dres, dx, part, nblocks, rows, groups, st);
-  else return cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+  if (rows > 0) {
+    if (ng <= 4) e = norm_dx_ng<4>(dy, x, w, rstd, dres, dx, rows, groups, st);
+    else if (ng <= 8) e = norm_dx_ng<8>(dy, x, w, rstd, dres, dx, rows, groups, st);
+    else if (ng <= 16) e = norm_dx_ng<16>(dy, x, w, rstd, dres, dx, rows, groups, st);
+    else if (ng <= 24) e = norm_dx_ng<24>(dy, x, w, rstd, dres, dx, rows, groups, st);
+    else return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+  }
+  rmsnorm_dw_kernel<<<nblocks, 256, 0, st>>>(static_cast<const uint4*>(dy), static_cast<const uint4*>(x), rstd, part,
+                                             rows, groups);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   column_sum_kernel<<<(hidden + 255) / 256, 256, 0, st>>>(part, dw, nblocks, hidden);
   return cudaGetLastError();

@@ -20,8 +20,9 @@ struct RowMap {
 cudaError_t launch_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int hidden,
                                float eps, cudaStream_t st);
 
-// dx = dres + RMSNorm'(dy); dw [hidden] fp32 = sum over rows of dy*x*r.
-// part is fp32 scratch of rmsnorm_bwd_blocks() * hidden floats.
+// dx = dres + RMSNorm'(dy) (row-parallel kernel); dw [hidden] fp32 = sum over
+// rows of dy*x*r (per-chunk partials, then a fixed-order column sum).  part is
+// fp32 scratch of rmsnorm_bwd_blocks() * hidden floats.
 cudaError_t launch_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, const void* dres,
                                void* dx, float* part, float* dw, int64_t rows, int hidden, cudaStream_t st);
 int rmsnorm_bwd_blocks();
