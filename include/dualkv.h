@@ -184,6 +184,19 @@ DUALKV_API int dualkv_bwd_static_workspace(const void* q, const void* k, const v
                                            float softmax_scale, int deterministic, int32_t num_splits, void* dq,
                                            void* dk, void* dv, void* stream);
 
+/*
+ * Self-test of the failure detection (no counterpart on the DualKV pages).
+ * Every pipeline wait in the kernels is bounded: a wait that does not
+ * complete within its limit records DUALKV_ERR_TIMEOUT and the wait's site id
+ * in the device error word, and the kernel returns instead of spinning.  This
+ * call launches one thread that makes such a wait on an mbarrier phase that
+ * nothing completes, with limit_ns (1 ns .. 10 s) and site (1 .. 2^24-1), so
+ * that the path can be exercised without breaking a real pipeline.  After it,
+ * dualkv_last_device_error() returns DUALKV_ERR_TIMEOUT and `site`.  Returns
+ * DUALKV_OK, DUALKV_ERR_INVALID_ARG or DUALKV_ERR_CUDA.
+ */
+DUALKV_API int dualkv_selftest_wait_timeout(int64_t limit_ns, int32_t site, void* stream);
+
 /* Static text for a dualkv_status value (never NULL). */
 DUALKV_API const char* dualkv_status_string(int status);
 

@@ -526,6 +526,14 @@ int dualkv_trace_read(double* ms, int64_t* launches, int32_t n) {
   return status;
 }
 
+int dualkv_selftest_wait_timeout(int64_t limit_ns, int32_t site, void* stream) {
+  if (limit_ns < 1 || limit_ns > 10000000000ll || site < 1 || site > 0xFFFFFF) return DUALKV_ERR_INVALID_ARG;
+  unsigned int* err = error_word_ptr();
+  if (!err) return DUALKV_ERR_CUDA;
+  return map_cuda(launch_wait_timeout_selftest(err, static_cast<uint64_t>(limit_ns), static_cast<uint32_t>(site),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 int dualkv_last_device_error(void* stream, int32_t* site) {
   if (site) *site = 0;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;

@@ -46,4 +46,8 @@ struct PromptMap {
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
                                  void* dk, void* dv, const PromptMap& map, int row_elems, cudaStream_t stream);
 
+// Self-test of the bounded waits: a wait on an mbarrier phase that never
+// completes gives up after limit_ns and records a timeout at `site`.
+cudaError_t launch_wait_timeout_selftest(unsigned int* err, uint64_t limit_ns, uint32_t site, cudaStream_t stream);
+
 }  // namespace dkv

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dkv {
 namespace {
@@ -84,6 +85,19 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
   }
 }
 
+// One thread waits, with the kernels' own bounded wait, for an mbarrier
+// phase that nothing completes; the wait gives up after limit_ns, records a
+// timeout at `site` in the error word and the kernel returns normally.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(unsigned int* err, uint64_t limit_ns,
+                                                                  uint32_t site) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, err, site, limit_ns);
+  }
+}
+
 int grid_for(int64_t work_threads) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -109,6 +123,11 @@ cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, in
     preprocess_kernel<8><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
                                                    Dvec, rows, static_cast<int>(T), Hq,
                                                    reinterpret_cast<float4*>(zero_ptr), z4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned int* err, uint64_t limit_ns, uint32_t site, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns, site);
   return cudaGetLastError();
 }
 

@@ -27,7 +27,7 @@ EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_st
             "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
             "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
-            "dualkv_packed_positions")
+            "dualkv_packed_positions", "dualkv_selftest_wait_timeout")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -100,6 +100,8 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_layer_bwd.restype = ctypes.c_int
     lib.dualkv_packed_positions.argtypes = [c_i32, p_i64, p_i32, p_i32, p_i32, c_i64]
     lib.dualkv_packed_positions.restype = ctypes.c_int
+    lib.dualkv_selftest_wait_timeout.argtypes = [c_i64, c_i32, c_p]
+    lib.dualkv_selftest_wait_timeout.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -240,6 +242,12 @@ def dualkv_last_device_error(stream=None):
     site = ctypes.c_int32(0)
     st = lib.dualkv_last_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def dualkv_selftest_wait_timeout(limit_ns: int, site: int, stream=None) -> None:
+    """Launches the bounded-wait self-test (a wait that nothing completes)."""
+    _check(lib.dualkv_selftest_wait_timeout(int(limit_ns), int(site), _stream(stream)),
+           "dualkv_selftest_wait_timeout")
 
 
 def dualkv_trace_enable(on: bool) -> None:

@@ -215,3 +215,10 @@ def test_layer_argument_errors(D):
                                                ctypes.byref(kw.get("gr", gr)), A, kw.get("nbytes", ws), None)
     assert bwd(gr=D.LayerGrads(*([A] * 5 + [None]))) == D.DUALKV_ERR_INVALID_ARG
     assert bwd(nbytes=16) == D.DUALKV_ERR_WORKSPACE
+
+
+def test_selftest_argument_errors(D):
+    assert D.lib.dualkv_selftest_wait_timeout(0, 5, None) == D.DUALKV_ERR_INVALID_ARG
+    assert D.lib.dualkv_selftest_wait_timeout(20_000_000_000, 5, None) == D.DUALKV_ERR_INVALID_ARG
+    assert D.lib.dualkv_selftest_wait_timeout(1000, 0, None) == D.DUALKV_ERR_INVALID_ARG
+    assert D.lib.dualkv_selftest_wait_timeout(1000, 1 << 24, None) == D.DUALKV_ERR_INVALID_ARG
