@@ -156,6 +156,8 @@ def to_f64(x: torch.Tensor) -> np.ndarray:
 LAYER_SHAPES = {
     "qwen3_8b": dict(hidden=4096, Hq=32, Hkv=8, d=128, inter=12288, rope_base=1.0e6, eps=1.0e-6),
     "small": dict(hidden=256, Hq=4, Hkv=2, d=64, inter=512, rope_base=1.0e4, eps=1.0e-6),
+    "small_d128": dict(hidden=512, Hq=4, Hkv=1, d=128, inter=256, rope_base=1.0e6, eps=1.0e-6),
+    "wide": dict(hidden=6144, Hq=2, Hkv=1, d=64, inter=256, rope_base=1.0e4, eps=1.0e-5),
 }
 
 

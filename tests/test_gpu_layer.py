@@ -46,8 +46,9 @@ def _setup(shape_name, groups, seed):
     return D, shape, cfg, w, wd, x, dy
 
 
-def test_layer_parity_against_oracle():
-    D, shape, cfg, w, wd, x, dy = _setup("small", GROUPS, 0)
+@pytest.mark.parametrize("shape_name", ["small", "small_d128", "wide"])
+def test_layer_parity_against_oracle(shape_name):
+    D, shape, cfg, w, wd, x, dy = _setup(shape_name, GROUPS, 0)
     layer = D.PackedLayer(cfg, wd, GROUPS)
     xg, dyg = x.cuda(), dy.cuda()
     y = layer.forward(xg)
