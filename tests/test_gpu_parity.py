@@ -133,14 +133,17 @@ def test_reduction_modes_agree():
 
 
 def test_peaked_scores_parity():
-    """Queries scaled by 8: scores spread over tens of units, so the running
-    maximum often jumps by more than 2^8 (log2 units) between key tiles and
-    the forward's rescale of O in TMEM runs; the backward sees near one-hot
-    rows."""
+    """Queries scaled by 8 and keys growing along the rows: the running
+    maximum often jumps by more than 2^8 (log2 units) between key tiles, so the
+    forward's rescale of O in TMEM runs; the backward sees near one-hot rows."""
     dk_ = _lib()
     w = synthetic.make_workload("peaked", 4, 2, 128, 300, (200, 0, 131, 128))
     x = synthetic.make_inputs(w, seed=11)
     x.q = (x.q.float() * 8).to(torch.bfloat16)
+    # keys grow along the rows, so later key tiles raise the row maximum: with
+    # these inputs about 40% of (row, key tile) steps after the first rescale O
+    grow = 1 + 4 * torch.arange(w.T, dtype=torch.float32)[:, None, None] / w.T
+    x.k = (x.k.float() * grow).to(torch.bfloat16)
     q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.dout))
     out, lse = dk_.forward(q, k, v, w.P, w.R_lens, w.scale)
     dq, dkk, dvv = dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=True, num_splits=2)
