@@ -257,9 +257,27 @@ def layer_leg(D, w, dev, stream):
     layouts = {"packed": ([(w.P, tuple(w.R_lens))], w.T, w.pairs_per_head()),
                "replicated": ([(w.P + int(r), ()) for r in w.R_lens], w.T_replicated,
                               w.pairs_per_head_replicated())}
+    # The replicated rows are gathered from the packed ones (sequence i =
+    # [prompt ; response i]).  A prompt row's dy is split evenly over the N
+    # sequences (exact for N a power of two); the shares add up to the packed
+    # dy, and no sequence gets all-zero rows, which would lower the power
+    # draw and flatter the replicated timing.
+    x_p = torch.randn((w.T, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
+    dy_p = torch.randn((w.T, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
+    offs = w.offsets
+    rep_idx = torch.cat([torch.cat([torch.arange(w.P), torch.arange(offs[i], offs[i] + int(r))])
+                         for i, r in enumerate(w.R_lens)]).to(dev)
+    results = {}
     for name, (groups, rows, pairs) in layouts.items():
-        x = torch.randn((rows, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
-        dy = torch.randn((rows, shape["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
+        if name == "packed":
+            x, dy = x_p, dy_p
+        else:
+            x, dy = x_p[rep_idx], dy_p[rep_idx]
+            share = (dy_p[:w.P].float() / w.N).to(torch.bfloat16)
+            start = 0
+            for r in w.R_lens:
+                dy[start:start + w.P] = share
+                start += w.P + int(r)
         layer = D.PackedLayer(cfg, weights, groups)
         y = torch.empty_like(x)
         dx = torch.empty_like(x)
@@ -297,7 +315,32 @@ def layer_leg(D, w, dev, stream):
                      "gemm_tflop": fl["gemm"] / 1e12, "attention_tflop": fl["attention"] / 1e12,
                      "tflops": (fl["gemm"] + fl["attention"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
                      "device_bytes": nbytes}
-        del layer, x, dy, y, dx, grads
+        if name == "packed":
+            results["packed"] = (y, dx, grads)
+        else:
+            # scatter the replicated results back to the packed rows
+            y_r = torch.empty_like(x_p, dtype=torch.float32)
+            dx_r = torch.zeros_like(x_p, dtype=torch.float32)
+            start = 0
+            for i, r in enumerate(w.R_lens):
+                r = int(r)
+                seq_y, seq_dx = y[start:start + w.P + r].float(), dx[start:start + w.P + r].float()
+                y_r[offs[i]:offs[i] + r] = seq_y[w.P:]
+                dx_r[offs[i]:offs[i] + r] = seq_dx[w.P:]
+                if i == 0:
+                    y_r[:w.P] = seq_y[:w.P]
+                dx_r[:w.P] += seq_dx[:w.P]
+                start += w.P + r
+            py, pdx, pg = results["packed"]
+
+            def rel(a, b):
+                return float((a.float() - b.float()).norm() / b.float().norm())
+
+            out["packed_vs_replicated_rel_l2"] = {
+                "y": rel(py, y_r), "dx": rel(pdx, dx_r),
+                "weight_grads_max": max(rel(pg[n], grads[n]) for n in pg)}
+            del y_r, dx_r
+        del layer, x, dy
         torch.cuda.empty_cache()
     out["speedup_packed"] = out["replicated"]["ms"] / out["packed"]["ms"]
     out["memory_reduction"] = 1.0 - out["packed"]["device_bytes"] / out["replicated"]["device_bytes"]
