@@ -22,7 +22,7 @@ section "Approach"; arXiv abstract page; forum page, "Two changes"):
   dQ/dK/dV are summed over the N sequences (the research-map page, "Approach":
   the shared prompt's gradients are accumulated across sequences).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * LSE is the natural log of sum_j exp(scale * q.k_j) (FlashAttention-2
   convention, the lineage named on the research-map page), layout [Hq, T].
