@@ -492,8 +492,10 @@ def main():
         step()
     tr = D.dualkv_trace_read()
     D.dualkv_trace_enable(False)
-    per_kernel = {name: (tot / cnt if cnt else 0.0) for name, (tot, cnt) in tr.items()}
-    launches_per_step = sum(cnt for _, cnt in tr.values()) // args.steps
+    # device time per step of each kernel (long work lists run as several launches)
+    per_kernel = {name: tot / args.steps for name, (tot, cnt) in tr.items()}
+    kernel_launches = {name: cnt // args.steps for name, (tot, cnt) in tr.items()}
+    launches_per_step = sum(kernel_launches.values())
 
     e2e = None
     if not args.kernels_only:
@@ -509,7 +511,8 @@ def main():
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
-    # dominant kernel: dK/dV (four products per unmasked pair: S^T, dP^T, dV, dK)
+    # dominant kernel: dK/dV (four products per unmasked pair: S^T, dP^T, dV, dK);
+    # per step, which is per launch whenever the work list fits one launch
     dkdv_ms = per_kernel.get("bwd_dkdv", 0.0)
     dkdv_flops = 8.0 * w.d * w.Hq * w.pairs_per_head()
     dkdv_tf = dkdv_flops / (dkdv_ms * 1e-3) / 1e12 if dkdv_ms else None
@@ -517,7 +520,8 @@ def main():
                 "unit": "TFLOP/s", "frac": (dkdv_tf / peak_sus) if dkdv_tf else None,
                 "traffic": recorded_traffic("dkdv_kernel", w.name, det),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
-                "algorithmic": "8*d flops per unmasked (query,key) pair per q-head"}
+                "algorithmic": "8*d flops per unmasked (query,key) pair per q-head",
+                "launches_per_step": kernel_launches.get("bwd_dkdv", 0)}
 
     # the two bandwidth-bound kernels of the backward, against the measured copy bandwidth
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -553,6 +557,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / peak_sus,
         "per_kernel_ms": per_kernel,
+        "kernel_launches_per_step": kernel_launches,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock_info,
         "e2e": e2e_obj,
