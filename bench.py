@@ -352,6 +352,58 @@ def layer_leg(D, w, dev, stream):
     return out
 
 
+def groups_leg(D, dev, stream):
+    """Four prompt groups (Qwen3-8B shapes: 32/8 heads, d 128; each group a
+    4096-token prompt and 8 responses of 4096 tokens) as one grouped forward +
+    backward, against four single-group calls on the same rows."""
+    Hq, Hkv, d, P, N, R = 32, 8, 128, 4096, 8, 4096
+    groups = [(P, (R,) * N)] * 4
+    T = synthetic.group_rows(groups)
+    scale = d ** -0.5
+    gen = torch.Generator(device=dev).manual_seed(5)
+    q, do = (torch.randn((T, Hq, d), device=dev, generator=gen).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn((T, Hkv, d), device=dev, generator=gen).to(torch.bfloat16) for _ in range(2))
+    out = torch.empty_like(q)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, False), dtype=torch.uint8,
+                     device=dev)
+    rows = P + N * R
+
+    def grouped():
+        D.dualkv_fwd_groups(q, k, v, groups, out, lse, scale, stream)
+        D.dualkv_bwd_groups(q, k, v, out, do, lse, groups, scale, False, ws, dq, dk, dv, stream=stream)
+
+    views = []
+    for g in range(4):
+        sl = slice(g * rows, (g + 1) * rows)
+        views.append([t[sl] for t in (q, k, v, out, do, dq, dk, dv)] + [lse[:, sl].contiguous()])
+
+    def separate():
+        for qq, kk, vv, oo, dd, dqq, dkk, dvv, ll in views:
+            D.dualkv_fwd(qq, kk, vv, P, (R,) * N, oo, ll, scale, stream)
+            D.dualkv_bwd(qq, kk, vv, oo, dd, ll, P, (R,) * N, scale, False, ws, dqq, dkk, dvv, stream=stream)
+
+    res = {"groups": 4, "P": P, "N": N, "R": R, "Hq": Hq, "Hkv": Hkv, "d": d, "T": T}
+    flops = 4 * synthetic.make_workload("g", Hq, Hkv, d, P, (R,) * N).useful_flops()
+    for name, fn in (("grouped", grouped), ("separate", separate)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(5):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 5
+        res[name] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    st, site = D.dualkv_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error {st} at wait site {site}")
+    return res
+
+
 # --------------------------------------------------------------------------- CPU oracle timings
 
 def _oracle_seq0_inputs(w: synthetic.Workload, seed: int):
@@ -437,6 +489,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
     ap.add_argument("--layer", action="store_true",
                     help="also time a Qwen3-8B-shaped decoder layer, packed against replicated")
+    ap.add_argument("--groups", action="store_true",
+                    help="also time four prompt groups in one call against four single-group calls")
     ap.add_argument("--kernels-only", action="store_true",
                     help="also skip the end-to-end leg (for profiling: one buffer set on the device)")
     args = ap.parse_args()
@@ -624,6 +678,9 @@ def main():
         st, site = D.dualkv_last_device_error(stream)
         if st != 0:
             raise RuntimeError(f"device error {st} at wait site {site}")
+
+    if rank == 0 and args.groups:
+        result["groups"] = groups_leg(D, dev, stream)
 
     if rank == 0 and args.layer:
         del q, k, v, do, out, lse, dq, dk, dv, ws

@@ -166,9 +166,19 @@ std::vector<uint32_t> query_items(const Sched& s) {
 
 // Sequence chunks of a prompt key tile's work: split c of group g covers its
 // responses [c*N_g/S, (c+1)*N_g/S); split 0 also takes the prompt's own queries.
+// Items are ordered group by group, longest first within each group: the
+// CTAs running together then come from one group and walk the same query
+// tiles, which L2 serves to all of them (ordering all groups' items by cost
+// alone made a four-group batch's dK/dV 8% slower than four separate calls).
 std::vector<uint32_t> key_items(const Sched& s, int S) {
+  std::vector<uint32_t> out;
   std::vector<CostItem> v;
   for (int seg = 0; seg < s.nseg; ++seg) {
+    if (s.prompt_of(seg) == seg && !v.empty()) {  // a new group starts
+      const std::vector<uint32_t> g = sorted_items(v);
+      out.insert(out.end(), g.begin(), g.end());
+      v.clear();
+    }
     const int nt = s.seg_tiles(seg);
     if (s.prompt_of(seg) == seg) {
       // Every (prompt key tile, split) is listed, even one whose sequence chunk
@@ -185,7 +195,9 @@ std::vector<uint32_t> key_items(const Sched& s, int S) {
       for (int j = 0; j < nt; ++j) v.push_back({nt - j, make_item(j, seg, 0)});
     }
   }
-  return sorted_items(v);
+  const std::vector<uint32_t> g = sorted_items(v);
+  out.insert(out.end(), g.begin(), g.end());
+  return out;
 }
 
 int auto_splits(const Shape& sh) {
