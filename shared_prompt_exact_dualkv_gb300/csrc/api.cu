@@ -63,7 +63,7 @@ int check_dims(int32_t Hq, int32_t Hkv, int32_t d) {
 
 int check_groups(Shape* sh, int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens, int32_t Hq,
                  int32_t Hkv, int32_t d) {
-  if (G < 1 || !P || !N) return DUALKV_ERR_INVALID_ARG;
+  if (G < 1 || G > kMaxSeg || !P || !N) return DUALKV_ERR_INVALID_ARG;
   int64_t nres = 0;
   for (int g = 0; g < G; ++g) {
     if (N[g] < 0 || P[g] < 0 || P[g] >= (int64_t(1) << 31)) return DUALKV_ERR_INVALID_ARG;

@@ -29,7 +29,7 @@ struct Groups {
 
 // Checks the group arrays (the attention entry points check them again).
 int check_groups(int32_t G, const int64_t* P, const int32_t* N, const int32_t* R, Groups* out) {
-  if (G < 1 || !P || !N) return DUALKV_ERR_INVALID_ARG;
+  if (G < 1 || G > kMaxSeg || !P || !N) return DUALKV_ERR_INVALID_ARG;
   int64_t T = 0, nres = 0;
   for (int g = 0; g < G; ++g) {
     if (P[g] < 0 || N[g] < 0) return DUALKV_ERR_INVALID_ARG;
