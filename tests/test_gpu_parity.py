@@ -72,7 +72,7 @@ def test_backward_parity(case, deterministic, oracle_results):
     w = synthetic.make_workload(*case)
     x, (q, k, v, do) = _device_inputs(w)
     out, lse = dk_.forward(q, k, v, w.P, w.R_lens, w.scale)
-    for splits in (0, 3):
+    for splits in (0, 3, 16):
         dq, dkk, dvv = dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale,
                                     deterministic=deterministic, num_splits=splits)
         st, site = dk_.dualkv_last_device_error()
