@@ -403,3 +403,48 @@ class PackedLayer:
         grads = {n: torch.empty(t.shape, dtype=torch.float32, device=t.device) for n, t in self.weights.items()}
         dualkv_layer_bwd(self.cfg, self.weights, x, dy, self.groups, dx, grads, self.workspace, stream)
         return dx, grads
+
+
+# --------------------------------------------------------------------------- autograd
+
+class DualKVAttention(torch.autograd.Function):
+    """torch.autograd wrapper of dualkv_fwd_groups / dualkv_bwd_groups.
+
+    forward(q, k, v, groups, softmax_scale, deterministic, num_splits) -> out;
+    the saved tensors are q, k, v, out and lse.  The backward's dout is made
+    contiguous before the call (the library's layouts are dense)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, groups, softmax_scale, deterministic, num_splits):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out, lse = forward_groups(q, k, v, groups, softmax_scale)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.groups, ctx.scale = groups, softmax_scale
+        ctx.deterministic, ctx.num_splits = deterministic, num_splits
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = backward_groups(q, k, v, out, dout.contiguous(), lse, ctx.groups, ctx.scale,
+                                     deterministic=ctx.deterministic, num_splits=ctx.num_splits)
+        return dq, dk, dv, None, None, None, None
+
+
+def dualkv_attention(q, k, v, P: Optional[int] = None, R_lens: Optional[Sequence[int]] = None, groups=None,
+                     softmax_scale: Optional[float] = None, deterministic: bool = False, num_splits: int = 0):
+    """Differentiable shared-prompt attention on packed rows.
+
+    Give either (P, R_lens) for one prompt group or ``groups`` = [(P_g,
+    R_lens_g), ...] for several.  q [T, Hq, d], k/v [T, Hkv, d] bf16 on the GPU;
+    returns out [T, Hq, d].  The gradient reaching a prompt row of out is the
+    gradient of the one shared row (its sequences' sum)."""
+    if groups is None:
+        if P is None or R_lens is None:
+            raise ValueError("give (P, R_lens) or groups")
+        groups = [(int(P), tuple(int(r) for r in R_lens))]
+    else:
+        groups = [(int(p), tuple(int(r) for r in rs)) for p, rs in groups]
+    if softmax_scale is None:
+        softmax_scale = q.shape[-1] ** -0.5
+    return DualKVAttention.apply(q, k, v, groups, float(softmax_scale), bool(deterministic), int(num_splits))
