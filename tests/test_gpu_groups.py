@@ -18,6 +18,8 @@ CASES = [
     ("mixed_d128", 4, 2, 128, [(300, (200, 0, 131)), (0, (77, 150)), (129, ()), (50, (1, 128))]),
     ("mixed_d64", 2, 1, 64, [(256, (129, 1)), (5, (3,)), (0, (0,)), (140, (40, 260, 7))]),
     ("eight_aligned", 4, 1, 128, [(128, (128, 128))] * 8),
+    # 16 groups + 1024 responses = 1040 segments, the per-call limit
+    ("max_segments", 2, 1, 64, [(40 + g, tuple((g + i) % 5 for i in range(64))) for g in range(16)]),
 ]
 
 

@@ -25,6 +25,7 @@ CASES = [
     ("short", 2, 1, 64, 5, (3, 2)),
     ("prompt_only", 2, 1, 128, 200, (0, 0)),
     ("many_seqs", 2, 1, 128, 130, tuple([1, 7, 33, 64, 127, 128, 129, 0] * 3)),
+    ("max_responses", 2, 1, 64, 130, tuple(i % 3 for i in range(1024))),   # N = 1024, the single-call limit
 ]
 
 
