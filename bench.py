@@ -577,6 +577,17 @@ def main():
                 "algorithmic": "8*d flops per unmasked (query,key) pair per q-head",
                 "launches_per_step": kernel_launches.get("bwd_dkdv", 0)}
 
+    # every tensor-core kernel against the measured sustained bf16 rate; executed
+    # flops per unmasked pair per q-head: forward 4d, dK/dV 8d, dQ 6d (S and dP
+    # recomputed)
+    tensor_kernels = {}
+    for name, per_pair in (("fwd", 4), ("bwd_dkdv", 8), ("bwd_dq", 6)):
+        kms = per_kernel.get(name, 0.0)
+        fl = per_pair * w.d * w.Hq * w.pairs_per_head()
+        tf = fl / (kms * 1e-3) / 1e12 if kms else None
+        tensor_kernels[name] = {"tflop_per_step": fl / 1e12, "ms": kms, "achieved_tflops": tf,
+                                "frac": (tf / peak_sus) if tf else None}
+
     # the two bandwidth-bound kernels of the backward, against the measured copy bandwidth
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     prompt_rows_bytes = w.P * w.Hkv * w.d * 4                      # one fp32 [P, Hkv, d] slice
@@ -616,6 +627,7 @@ def main():
         "clocks": clock_info,
         "e2e": e2e_obj,
         "roofline": roofline,
+        "tensor_kernels": tensor_kernels,
         "hbm_kernels": hbm_kernels,
     }
 
