@@ -69,23 +69,37 @@ __host__ __device__ inline int fwd_head_slots(int Hq, int group) { return (group
 // >= lim are excluded (lim = 128 on unmasked tiles).
 template <bool MASKED>
 __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
-  float mx[8];
+  if constexpr (!MASKED) {
+    // the TMEM load reduces each thread's 32 columns itself
+    float m = -INFINITY;
 #pragma unroll
-  for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-    uint32_t r[64];
-    tmem_ld32(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-    tmem_ld32(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float v0 = (!MASKED || hc * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY;
-      const float v1 = (!MASKED || hc * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY;
-      mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], v0, v1);
+    for (int hc = 0; hc < 2; ++hc) {
+      uint32_t r[64];
+      const float m0 = tmem_ld32_max(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      const float m1 = tmem_ld32_max(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      tmem_ld_wait();
+      m = fmax3(m, m0, m1);
     }
+    return m;
+  } else {
+    float mx[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      uint32_t r[64];
+      tmem_ld32(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      tmem_ld32(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float v0 = (hc * 64 + i < lim) ? __uint_as_float(r[i]) : -INFINITY;
+        const float v1 = (hc * 64 + i + 1 < lim) ? __uint_as_float(r[i + 1]) : -INFINITY;
+        mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], v0, v1);
+      }
+    }
+    return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
   }
-  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 }
 
 // P = exp2(c*S - m_sub) as bf16 written over the first 64 columns of S.
