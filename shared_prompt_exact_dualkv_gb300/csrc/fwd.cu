@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kSFull + i], 1);
-      mbar_init(&bar[kPFull + i], kHeadThreads);
+      mbar_init(&bar[kPFull + i], kHeadThreads / 32);  // one arrival per softmax warp
       mbar_init(&bar[kODone + i], 1);
     }
     fence_mbar_init();
@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(320, 1)
       m_use = m_new;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[kPFull + x]);
+      __syncwarp();  // every lane's P (and rescaled O) is stored and fenced
+      if (lane == 0) mbar_arrive(&bar[kPFull + x]);
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bar[kODone + x], 0, err, 303);
