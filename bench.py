@@ -50,6 +50,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def blas_threads():
+    """Threads of the BLAS that numpy calls (the oracle's matrix products):
+    threadpoolctl if installed, else the OpenBLAS thread query of the loaded
+    library, else None."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except ImportError:
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ln.split()[-1].startswith("/")})
+    except OSError:
+        return None
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -576,6 +606,14 @@ def main():
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
                 "algorithmic": "8*d flops per unmasked (query,key) pair per q-head",
                 "launches_per_step": kernel_launches.get("bwd_dkdv", 0)}
+    # The measured sustained rate was taken at the clock its own run settled
+    # at; compare per MHz of sampled SM clock as well.
+    peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    run_mhz = clock_info.get("sm_mhz")
+    if dkdv_tf and peak_mhz and run_mhz:
+        roofline["per_mhz"] = {"achieved_tflops_per_mhz": dkdv_tf / run_mhz, "run_sm_mhz": run_mhz,
+                               "peak_tflops_per_mhz": peak_sus / peak_mhz, "peak_sm_mhz": peak_mhz,
+                               "frac": (dkdv_tf / run_mhz) / (peak_sus / peak_mhz)}
 
     # every tensor-core kernel against the measured sustained bf16 rate; executed
     # flops per unmasked pair per q-head: forward 4d, dK/dV 8d, dQ 6d (S and dP
@@ -682,11 +720,19 @@ def main():
         torch.cuda.empty_cache()
         if world == 1:
             dt, fl = oracle_sample_seconds(w)
+            # The replicated oracle's cost is linear in heads and, per sequence,
+            # in its causal pairs: scale the one (head, sequence) sample to the
+            # whole step.
+            seq0_pairs = (w.P + w.R_lens[0]) * (w.P + w.R_lens[0] + 1) // 2
+            full_s = dt * w.Hq * w.pairs_per_head_replicated() / seq0_pairs
             result["cpu_baseline"] = {
                 "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                "seconds": dt,
+                "blas_threads": blas_threads(), "seconds": dt,
                 "sample": f"fp64 oracle fwd+bwd of q-head 0 on sequence 0 ([prompt; response_0], "
-                          f"{w.P + w.R_lens[0]} rows); BLAS multithreaded, elementwise single-threaded"}
+                          f"{w.P + w.R_lens[0]} rows); BLAS multithreaded, elementwise single-threaded",
+                "extrapolated_step_seconds": full_s,
+                "extrapolation": f"extrapolated, not measured: sample seconds x {w.Hq} q-heads x "
+                                 f"(causal pairs of all {w.N} replicated sequences / pairs of sequence 0)"}
         st, site = D.dualkv_last_device_error(stream)
         if st != 0:
             raise RuntimeError(f"device error {st} at wait site {site}")

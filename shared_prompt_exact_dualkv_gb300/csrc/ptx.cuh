@@ -13,7 +13,7 @@
 namespace dkv {
 
 // ------------------------------------------------------------------ errors
-// Device error word layout: low 8 bits = error kind, bits 8..23 = site id.
+// Device error word layout: bits 0..7 = error kind, bits 8..31 = site id (24 bits).
 enum : uint32_t { kDevErrTimeout = 6u };
 
 struct DevErr {
@@ -21,7 +21,7 @@ struct DevErr {
 };
 
 __device__ __forceinline__ void record_error(unsigned int* word, uint32_t kind, uint32_t site) {
-  if (word) atomicCAS(word, 0u, kind | (site << 8));
+  if (word) atomicCAS(word, 0u, (kind & 0xFFu) | ((site & 0xFFFFFFu) << 8));
 }
 
 // ------------------------------------------------------------------ basics

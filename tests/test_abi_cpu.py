@@ -222,3 +222,26 @@ def test_selftest_argument_errors(D):
     assert D.lib.dualkv_selftest_wait_timeout(20_000_000_000, 5, None) == D.DUALKV_ERR_INVALID_ARG
     assert D.lib.dualkv_selftest_wait_timeout(1000, 0, None) == D.DUALKV_ERR_INVALID_ARG
     assert D.lib.dualkv_selftest_wait_timeout(1000, 1 << 24, None) == D.DUALKV_ERR_INVALID_ARG
+
+
+def test_static_scratch_limit_matches_header_constant(D):
+    """STATIC_SCRATCH_BYTES in the binding is DUALKV_STATIC_SCRATCH_BYTES of the
+    header, and the library refuses exactly the shapes whose workspace exceeds
+    it (on a machine without a GPU an accepted shape fails later, at the
+    device lookup, with another status)."""
+    text = open(HEADERS[0]).read()
+    m = re.search(r"#define DUALKV_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == D.STATIC_SCRATCH_BYTES
+    R = (ctypes.c_int32 * 1)(0)
+
+    def need(P):
+        return D.lib.dualkv_bwd_workspace_bytes(P, 1, R, 1, 1, 64, 0, 0)
+
+    lo, hi = 1, 1 << 20
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= D.STATIC_SCRATCH_BYTES else (lo, mid)
+    call = lambda P: D.lib.dualkv_bwd_static_workspace(None, None, None, None, None, None, P, 1, R, 1, 1, 64,
+                                                       0.125, 0, 0, None, None, None, None)
+    assert call(hi) == D.DUALKV_ERR_WORKSPACE
+    assert call(lo) != D.DUALKV_ERR_WORKSPACE

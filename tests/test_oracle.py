@@ -296,6 +296,71 @@ def test_sampled_rows_match_full_oracle():
             np.testing.assert_allclose(svd, dv[keys, j], atol=1e-12)
 
 
+# --------------------------------------------------------------------------- kv-group oracle (torch fp64)
+
+@pytest.mark.parametrize("P,R_lens,Hq,Hkv,d,row_block", [
+    (70, [33, 0, 50, 7], 4, 2, 8, 16),      # ragged, an empty response, blocks inside segments
+    (0, [40, 17], 2, 1, 8, 16),             # P = 0: independent causal sequences
+    (45, [0], 2, 2, 4, 8),                  # a prompt alone
+    (33, [64], 6, 2, 8, 64),                # N = 1, group of 3 q-heads
+])
+def test_kvgroup_oracle_matches_numpy_oracle(P, R_lens, Hq, Hkv, d, row_block):
+    """The torch kv-group evaluation (prompt rows once, responses against
+    prompt + own keys) equals the replicated NumPy oracle to fp64 rounding,
+    for every output, including complete row ranges through kvgroup_rows."""
+    from oracle import kvgroup as okg
+    q, k, v, do = rand_case(P, R_lens, Hq, Hkv, d, seed=12)
+    scale = 1 / math.sqrt(d)
+    out, lse = ora.dualkv_forward(q, k, v, P, R_lens, scale)
+    dq, dk, dv = ora.dualkv_backward(q, k, v, do, P, R_lens, scale)
+    g = Hq // Hkv
+    T = P + sum(R_lens)
+    off = ora.segment_offsets(P, R_lens)
+    ranges = [(a, min(a + 16, b)) for a, b in ([(0, P)] + [(off[i], off[i + 1]) for i in range(len(R_lens))]) if b > a]
+    for j in range(Hkv):
+        hs = slice(j * g, (j + 1) * g)
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+        r = okg.kvgroup_forward_backward(t(q[:, hs]), t(k[:, j]), t(v[:, j]), t(do[:, hs]), P, R_lens, scale,
+                                         row_block=row_block)
+        np.testing.assert_allclose(r["out"].numpy(), out[:, hs], atol=1e-12)
+        np.testing.assert_allclose(r["lse"].numpy(), lse[hs], atol=1e-12)
+        np.testing.assert_allclose(r["dq"].numpy(), dq[:, hs], atol=1e-12)
+        np.testing.assert_allclose(r["dk"].numpy(), dk[:, j], atol=1e-12)
+        np.testing.assert_allclose(r["dv"].numpy(), dv[:, j], atol=1e-12)
+        f = okg.kvgroup_forward_backward(t(q[:, hs]), t(k[:, j]), t(v[:, j]), None, P, R_lens, scale)
+        np.testing.assert_allclose(f["out"].numpy(), out[:, hs], atol=1e-12)
+        rr = okg.kvgroup_rows(t(q[:, hs]), t(k[:, j]), t(v[:, j]), t(do[:, hs]), P, R_lens, scale, ranges,
+                              row_block=5)
+        for a, b in ranges:
+            np.testing.assert_allclose(rr[(a, b)]["out"].numpy(), out[a:b, hs].transpose(1, 0, 2), atol=1e-12)
+            np.testing.assert_allclose(rr[(a, b)]["lse"].numpy(), lse[hs, a:b], atol=1e-12)
+            np.testing.assert_allclose(rr[(a, b)]["dq"].numpy(), dq[a:b, hs].transpose(1, 0, 2), atol=1e-12)
+    assert T == off[-1]
+
+
+def test_kvgroup_oracle_catches_a_dropped_response_key():
+    """A kv-group evaluation that leaves out a response row's own diagonal key
+    disagrees with the replicated oracle (the comparison above can fail)."""
+    from oracle import kvgroup as okg
+    P, R_lens, Hq, Hkv, d = 20, [9, 13], 2, 1, 6
+    q, k, v, do = rand_case(P, R_lens, Hq, Hkv, d, seed=13)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+    real = okg._block_fwd
+
+    def no_diag(qb, kk, vv, scale, vis, n_open=0):
+        b = vis.shape[0]
+        vis = vis & ~torch.eye(b, vis.shape[1], dtype=torch.bool, device=vis.device).roll(vis.shape[1] - b, 1)
+        return real(qb, kk, vv, scale, vis, n_open)
+
+    out, _ = ora.dualkv_forward(q, k, v, P, R_lens, 0.4)
+    okg._block_fwd = no_diag
+    try:
+        r = okg.kvgroup_forward_backward(t(q), t(k[:, 0]), t(v[:, 0]), None, P, R_lens, 0.4, row_block=4)
+    finally:
+        okg._block_fwd = real
+    assert not np.allclose(r["out"].numpy(), out, atol=1e-3)   # NaN rows (nothing visible) also fail
+
+
 # --------------------------------------------------------------------------- planted mistakes
 
 def _mutant(monkeypatch, fwd=None, bwd=None):

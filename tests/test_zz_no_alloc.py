@@ -58,3 +58,25 @@ def test_static_workspace_rejects_oversize_shape():
     st = D.lib.dualkv_bwd_static_workspace(None, None, None, None, None, None, 65536, 1, R, 32, 8, 128, 0.088,
                                            0, 0, None, None, None, None)
     assert st == D.DUALKV_ERR_WORKSPACE
+
+
+def test_static_workspace_limit_is_the_library_constant():
+    """The Python constant STATIC_SCRATCH_BYTES is the library's own limit: a
+    shape whose workspace is the largest at or below it is accepted, and the
+    next larger shape (one more prompt row) is refused with
+    DUALKV_ERR_WORKSPACE before any launch (null data pointers: nothing runs)."""
+    from shared_prompt_exact_dualkv_gb300 import dualkv as D
+    R = (ctypes.c_int32 * 1)(0)
+
+    def need(P):
+        return D.lib.dualkv_bwd_workspace_bytes(P, 1, R, 1, 1, 64, 0, 0)
+
+    lo, hi = 1, 1 << 20                      # need(lo) <= limit < need(hi)
+    assert need(lo) <= D.STATIC_SCRATCH_BYTES < need(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= D.STATIC_SCRATCH_BYTES else (lo, mid)
+    call = lambda P: D.lib.dualkv_bwd_static_workspace(None, None, None, None, None, None, P, 1, R, 1, 1, 64,
+                                                       0.125, 0, 0, None, None, None, None)
+    assert call(hi) == D.DUALKV_ERR_WORKSPACE
+    assert call(lo) == D.DUALKV_ERR_INVALID_ARG   # accepted size; the null pointers are refused next
