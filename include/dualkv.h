@@ -153,6 +153,53 @@ DUALKV_API int dualkv_bwd_groups(const void* q, const void* k, const void* v, co
                                  void* dq, void* dk, void* dv, void* stream);
 
 /*
+ * One rank's part of a sequence-sharded step (research-map page, "Approach":
+ * the shared prompt's gradients are accumulated across the N sequences in
+ * fp32; "Key results" compares DualKV with sequence parallelism but the
+ * pages describe no sharded DualKV).  When the N responses of a prompt are
+ * spread over several ranks, every rank holds the whole prompt and its own
+ * responses, packed as [prompt ; its responses], and these two calls let the
+ * ranks divide the prompt's own causal attention instead of repeating it:
+ * a rank takes the prompt query rows [prompt_row_lo, prompt_row_hi) and all
+ * of its responses' query rows.  The responses need only the prompt's keys
+ * and values, which every rank holds.
+ *   prompt_row_lo, prompt_row_hi : 0 <= lo <= hi <= P; each a multiple of
+ *                   128 or equal to P.  (0, P) takes the whole prompt, (P, P)
+ *                   none of it.  Other values: DUALKV_ERR_INVALID_ARG.
+ *
+ * dualkv_fwd_partial: as dualkv_fwd, except that out and lse are written
+ *   only for the prompt rows in [lo, hi) and for the response rows; the other
+ *   prompt rows are left untouched (another rank computes them).
+ *
+ * dualkv_bwd_partial: as dualkv_bwd, except that
+ *   - only the prompt query rows in [lo, hi) take part: the other prompt
+ *     rows are treated as rows whose output gradient is zero, and their rows
+ *     of dq (and dq_prompt) are left untouched.  dout, out and lse need to be
+ *     valid only for the rows that take part;
+ *   - the prompt rows' gradients are also returned unrounded, in fp32, when
+ *     the pointers are not NULL (each may be NULL independently):
+ *       dq_prompt : device [P, Hq, d] fp32, rows [lo, hi) written;
+ *       dk_prompt, dv_prompt : device [P, Hkv, d] fp32, every prompt row
+ *                   written with this call's sum over its query rows.
+ *     Summing these over the ranks (in fp32) and rounding once gives the
+ *     sharded step's prompt gradients; the bf16 prompt rows of dq/dk/dv hold
+ *     this call's partial sums rounded to bf16.
+ *   The workspace is sized by dualkv_bwd_workspace_bytes() for the same
+ *   shape, mode and split count.  With (lo, hi) = (0, P) the bf16 outputs are
+ *   those of dualkv_bwd.  Every fp32 pointer must be 16-byte aligned.
+ */
+DUALKV_API int dualkv_fwd_partial(const void* q, const void* k, const void* v, int64_t P, int32_t N,
+                                  const int32_t* R_lens, int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale,
+                                  int64_t prompt_row_lo, int64_t prompt_row_hi, void* out, float* lse,
+                                  void* stream);
+DUALKV_API int dualkv_bwd_partial(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                  const float* lse, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
+                                  int32_t Hkv, int32_t d, float softmax_scale, int deterministic,
+                                  int32_t num_splits, int64_t prompt_row_lo, int64_t prompt_row_hi,
+                                  void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv,
+                                  float* dq_prompt, float* dk_prompt, float* dv_prompt, void* stream);
+
+/*
  * Backward pass without any allocation (the DualKV pages have no counterpart;
  * this entry point exists for callers of this library, not for the method).
  * Some callers cannot call cudaMalloc or ask an allocator for memory at the

@@ -118,6 +118,8 @@ void fill_common(Sched* s, const Shape& sh, float scale) {
   s->scale_log2 = scale * 1.4426950408889634f;
   s->num_splits = 1;
   s->num_items = 0;
+  s->pq_lo = 0;
+  s->pq_hi = 0xFFFF;
   int seg = 0, r = 0;
   int32_t row = 0, acc = 0;
   for (size_t g = 0; g < sh.P.size(); ++g) {
@@ -153,13 +155,17 @@ std::vector<uint32_t> sorted_items(std::vector<CostItem>& v) {
 }
 
 // Query-tile items (forward and dQ): cost = number of key tiles walked.
+// Prompt query tiles outside [pq_lo, pq_hi) are not listed.
 std::vector<uint32_t> query_items(const Sched& s) {
   std::vector<CostItem> v;
   for (int seg = 0; seg < s.nseg; ++seg) {
     const int p = s.prompt_of(seg);
     const int nt = s.seg_tiles(seg);
     const int nA = (p == seg) ? 0 : s.seg_tiles(p);
-    for (int t = 0; t < nt; ++t) v.push_back({nA + t + 1, make_item(t, seg, 0)});
+    for (int t = 0; t < nt; ++t) {
+      if (p == seg && (t < s.pq_lo || t >= s.pq_hi)) continue;
+      v.push_back({nA + t + 1, make_item(t, seg, 0)});
+    }
   }
   return sorted_items(v);
 }
@@ -187,7 +193,8 @@ std::vector<uint32_t> key_items(const Sched& s, int S) {
       const int ng = s.responses_of(seg);
       for (int j = 0; j < nt; ++j)
         for (int c = 0; c < S; ++c) {
-          int64_t cost = (c == 0) ? (nt - j) : 0;
+          // split 0 also walks the prompt's own query tiles j.. within [pq_lo, pq_hi)
+          int64_t cost = (c == 0) ? std::max(0, std::min(nt, s.pq_hi) - std::max(j, s.pq_lo)) : 0;
           for (int i = seg + 1 + (c * ng) / S; i < seg + 1 + ((c + 1) * ng) / S; ++i) cost += s.seg_tiles(i);
           v.push_back({cost, make_item(j, seg, c)});
         }
@@ -340,8 +347,22 @@ PromptMap* make_prompt_map(const Shape& sh) {
   return m;
 }
 
+// Prompt query tiles a call takes part in: [lo, hi) in tiles of kTile rows.
+struct PromptPart {
+  int32_t lo = 0, hi = 0xFFFF;
+};
+
+// Rows [row_lo, row_hi) of a prompt of P rows, tile-aligned (either end may be P).
+int prompt_part(PromptPart* part, int64_t P, int64_t row_lo, int64_t row_hi) {
+  if (row_lo < 0 || row_hi < row_lo || row_hi > P) return DUALKV_ERR_INVALID_ARG;
+  if ((row_lo % kTile != 0 && row_lo != P) || (row_hi % kTile != 0 && row_hi != P)) return DUALKV_ERR_INVALID_ARG;
+  part->lo = static_cast<int32_t>((row_lo + kTile - 1) / kTile);
+  part->hi = static_cast<int32_t>((row_hi + kTile - 1) / kTile);
+  return DUALKV_OK;
+}
+
 int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float scale, void* out, float* lse,
-             void* stream) {
+             void* stream, PromptPart part = PromptPart()) {
   if (!std::isfinite(scale)) return DUALKV_ERR_INVALID_ARG;
   if (sh.T == 0) return DUALKV_OK;
   if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID_ARG;
@@ -349,6 +370,8 @@ int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float
     return DUALKV_ERR_ALIGNMENT;
   std::unique_ptr<Sched> s(new Sched);
   fill_common(s.get(), sh, scale);
+  s->pq_lo = part.lo;
+  s->pq_hi = part.hi;
   const std::vector<uint32_t> items = query_items(*s);
   CUtensorMap mQ, mK, mV;
   if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
@@ -363,14 +386,23 @@ int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float
   }));
 }
 
+// fp32 copies of the prompt rows' gradients (accumulator row order), or nulls.
+struct PromptF32 {
+  float* dq = nullptr;
+  float* dk = nullptr;
+  float* dv = nullptr;
+};
+
 int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const void* out, const void* dout,
              const float* lse, float scale, int deterministic, int32_t num_splits, void* workspace,
-             size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream) {
+             size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream, PromptPart part = PromptPart(),
+             PromptF32 f32 = PromptF32()) {
   if (!std::isfinite(scale)) return DUALKV_ERR_INVALID_ARG;
   if (sh.T == 0) return DUALKV_OK;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return DUALKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(f32.dq) ||
+      !aligned16(f32.dk) || !aligned16(f32.dv))
     return DUALKV_ERR_ALIGNMENT;
   const int det = deterministic ? 1 : 0;
   const int S = resolve_splits(sh, num_splits);
@@ -382,6 +414,8 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   fill_common(sq.get(), sh, scale);
   fill_common(sk.get(), sh, scale);
   sk->num_splits = S;
+  sq->pq_lo = sk->pq_lo = part.lo;
+  sq->pq_hi = sk->pq_hi = part.hi;
   const std::vector<uint32_t> q_items = query_items(*sq);
   const std::vector<uint32_t> k_items = key_items(*sk, S);
   std::unique_ptr<PromptMap> map(make_prompt_map(sh));
@@ -412,12 +446,12 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
     });
   if (e == cudaSuccess && map->ngroups > 0) {
     TraceScope ts(3, cs);
-    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, *map, sh.Hkv * sh.d, cs);
+    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, f32.dk, f32.dv, *map, sh.Hkv * sh.d, cs);
   }
   if (e == cudaSuccess)
     e = launch_chunks(sq.get(), q_items, [&](const Sched& c) {
       TraceScope ts(4, cs);
-      return launch_dq(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dq, err, cs);
+      return launch_dq(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dq, f32.dq, err, cs);
     });
   return map_cuda(e);
 }
@@ -497,6 +531,37 @@ int dualkv_bwd_groups(const void* q, const void* k, const void* v, const void* o
   if (st != DUALKV_OK) return st;
   return bwd_impl(sh, q, k, v, out, dout, lse, softmax_scale, deterministic, num_splits, workspace,
                   workspace_bytes, dq, dk, dv, stream);
+}
+
+int dualkv_fwd_partial(const void* q, const void* k, const void* v, int64_t P, int32_t N, const int32_t* R_lens,
+                       int32_t Hq, int32_t Hkv, int32_t d, float softmax_scale, int64_t prompt_row_lo,
+                       int64_t prompt_row_hi, void* out, float* lse, void* stream) {
+  Shape sh;
+  int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
+  if (st != DUALKV_OK) return st;
+  PromptPart part;
+  st = prompt_part(&part, P, prompt_row_lo, prompt_row_hi);
+  if (st != DUALKV_OK) return st;
+  return fwd_impl(sh, q, k, v, softmax_scale, out, lse, stream, part);
+}
+
+int dualkv_bwd_partial(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                       const float* lse, int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq, int32_t Hkv,
+                       int32_t d, float softmax_scale, int deterministic, int32_t num_splits, int64_t prompt_row_lo,
+                       int64_t prompt_row_hi, void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv,
+                       float* dq_prompt, float* dk_prompt, float* dv_prompt, void* stream) {
+  Shape sh;
+  int st = check_shape(&sh, P, N, R_lens, Hq, Hkv, d);
+  if (st != DUALKV_OK) return st;
+  PromptPart part;
+  st = prompt_part(&part, P, prompt_row_lo, prompt_row_hi);
+  if (st != DUALKV_OK) return st;
+  PromptF32 f32;
+  f32.dq = dq_prompt;
+  f32.dk = dk_prompt;
+  f32.dv = dv_prompt;
+  return bwd_impl(sh, q, k, v, out, dout, lse, softmax_scale, deterministic, num_splits, workspace,
+                  workspace_bytes, dq, dk, dv, stream, part, f32);
 }
 
 int dualkv_trace_enable(int on) {

@@ -93,7 +93,8 @@ struct QRuns {
       seq_lo = seg + 1 + (split * ng) / s.num_splits;
       const int seq_hi = seg + 1 + ((split + 1) * ng) / s.num_splits;
       num_runs = has_prompt + (seq_hi - seq_lo);
-      if (has_prompt) per_head += nP - j;
+      // the prompt's own query tiles j..nP-1 (causal), within the part taken
+      if (has_prompt) per_head += max(0, min(nP, s.pq_hi) - max(j, s.pq_lo));
       for (int i = seq_lo; i < seq_hi; ++i) per_head += s.seg_tiles(i);
       acc0 = s.acc_row[seg] + j * kTile;
     } else {
@@ -109,25 +110,24 @@ struct QRuns {
 
 struct QIter {
   int32_t hh, r, t;
-  int32_t q_first, t_begin, t_end, seg_end;
-  bool diag_first;
+  int32_t q_first, t_end, seg_end;
+  int32_t diag_t;   // the query tile on the key tile's diagonal (-1: none in this run)
 
   __device__ __forceinline__ void load_run(const Sched& s, const QRuns& R) {
     if (R.has_prompt && r == 0) {
       q_first = s.off[R.seg];
-      t_begin = R.j;
-      t_end = R.nP;
+      t = max(R.j, s.pq_lo);
+      t_end = min(R.nP, s.pq_hi);
       seg_end = s.off[R.seg + 1];
-      diag_first = true;
+      diag_t = R.j;
     } else {
       const int i = R.seq_lo + r - R.has_prompt;
       q_first = s.off[i];
-      t_begin = R.prompt_item ? 0 : R.j;
+      t = R.prompt_item ? 0 : R.j;
       t_end = s.seg_tiles(i);
       seg_end = s.off[i + 1];
-      diag_first = !R.prompt_item;
+      diag_t = R.prompt_item ? -1 : R.j;
     }
-    t = t_begin;
   }
   __device__ __forceinline__ void skip_empty(const Sched& s, const QRuns& R) {
     while (t >= t_end) {
@@ -150,7 +150,7 @@ struct QIter {
     skip_empty(s, R);
   }
   __device__ __forceinline__ int32_t q0() const { return q_first + t * kTile; }
-  __device__ __forceinline__ bool diag() const { return diag_first && t == t_begin; }
+  __device__ __forceinline__ bool diag() const { return t == diag_t; }
   __device__ __forceinline__ int32_t head(const QRuns& R) const { return R.hk * R.group + hh; }
 };
 

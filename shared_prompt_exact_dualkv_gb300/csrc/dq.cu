@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(320, 1)
     dq_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
               const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
               const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
-              const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, unsigned int* err) {
+              const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, float* __restrict__ dq_prompt,
+              unsigned int* err) {
   using L = DqLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,6 +284,13 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const bool valid = q < w.q_end;
       uint4* dst = reinterpret_cast<uint4*>(dq + (static_cast<size_t>(q) * s.Hq + h) * D + half * (D / 2));
+      // A prompt row's fp32 dQ also goes to dq_prompt (accumulator row order,
+      // [prompt rows of all groups, Hq, D]) when the caller asked for it.
+      const int32_t seg = static_cast<int32_t>(item_seg(item));
+      float4* dst32 = nullptr;
+      if (dq_prompt != nullptr && s.prompt_of(seg) == seg)
+        dst32 = reinterpret_cast<float4*>(
+            dq_prompt + (static_cast<size_t>(s.acc_row[seg] + (q - s.off[seg])) * s.Hq + h) * D + half * (D / 2));
 #pragma unroll
       for (int ci = 0; ci < D / 64; ++ci) {
         uint32_t r[32];
@@ -295,6 +303,12 @@ __global__ void __launch_bounds__(320, 1)
         if (valid) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          if (dst32 != nullptr) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst32[ci * 8 + v] = make_float4(__uint_as_float(r[4 * v]) * s.scale, __uint_as_float(r[4 * v + 1]) * s.scale,
+                                              __uint_as_float(r[4 * v + 2]) * s.scale, __uint_as_float(r[4 * v + 3]) * s.scale);
+          }
         }
       }
     }
@@ -311,24 +325,25 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D>
 cudaError_t launch_dq_d(const Sched& s, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                        const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, unsigned int* err,
-                        cudaStream_t stream) {
+                        const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, float* dq_prompt,
+                        unsigned int* err, cudaStream_t stream) {
   using L = DqLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hq);
-  dq_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dq), err);
+  dq_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dq),
+                                                 dq_prompt, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dq(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
-                      const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, unsigned int* err,
-                      cudaStream_t stream) {
+                      const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dq, float* dq_prompt,
+                      unsigned int* err, cudaStream_t stream) {
   if (s.num_items == 0) return cudaSuccess;
-  return d == 64 ? launch_dq_d<64>(s, mQ, mK, mV, mdO, lse, Dvec, dq, err, stream)
-                 : launch_dq_d<128>(s, mQ, mK, mV, mdO, lse, Dvec, dq, err, stream);
+  return d == 64 ? launch_dq_d<64>(s, mQ, mK, mV, mdO, lse, Dvec, dq, dq_prompt, err, stream)
+                 : launch_dq_d<128>(s, mQ, mK, mV, mdO, lse, Dvec, dq, dq_prompt, err, stream);
 }
 
 }  // namespace dkv

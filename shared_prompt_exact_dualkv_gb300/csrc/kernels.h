@@ -19,9 +19,11 @@ cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, in
                               float* zero_ptr, size_t zero_n, cudaStream_t stream);
 
 // dQ: one (query tile, q-head) item per CTA, same key walk as the forward.
+// When `dq_prompt` is not null, prompt rows are also written there in fp32
+// ([prompt rows of all groups in accumulator order, Hq, d]).
 cudaError_t launch_dq(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK,
                       const CUtensorMap& mV, const CUtensorMap& mdO, const float* lse, const float* Dvec,
-                      void* dq, unsigned int* err, cudaStream_t stream);
+                      void* dq, float* dq_prompt, unsigned int* err, cudaStream_t stream);
 
 // dK/dV: one (key tile, kv-head, split) item per CTA.  Response key rows are
 // written to dk/dv (bf16); prompt key rows go to fp32 `acc_k/acc_v`
@@ -42,9 +44,12 @@ struct PromptMap {
 
 // Prompt rows of dK/dV: sum the `nsplit` fp32 slices (stride `slice` floats)
 // of the accumulator in split order and round to bf16 (RNE) into the
-// prompt rows of dk/dv (row_elems = Hkv * d values per row).
+// prompt rows of dk/dv (row_elems = Hkv * d values per row).  When f32_k /
+// f32_v are not null, the fp32 sums are also stored there, in accumulator
+// row order ([prompt rows of all groups, Hkv, d]).
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
-                                 void* dk, void* dv, const PromptMap& map, int row_elems, cudaStream_t stream);
+                                 void* dk, void* dv, float* f32_k, float* f32_v, const PromptMap& map,
+                                 int row_elems, cudaStream_t stream);
 
 // Self-test of the bounded waits: a wait on an mbarrier phase that never
 // completes gives up after limit_ns and records a timeout at `site`.

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
                                                             const float4* __restrict__ src_k,
                                                             const float4* __restrict__ src_v, int nsplit,
                                                             int64_t slice4, uint2* __restrict__ dk,
-                                                            uint2* __restrict__ dv, int row4) {
+                                                            uint2* __restrict__ dv, float4* __restrict__ f32_k,
+                                                            float4* __restrict__ f32_v, int row4) {
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
   const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
@@ -81,6 +82,8 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
       pk.x = *reinterpret_cast<uint32_t*>(&lo2);
       pk.y = *reinterpret_cast<uint32_t*>(&hi2);
       (which ? dv : dk)[out] = pk;
+      float4* f32 = which ? f32_v : f32_k;
+      if (f32 != nullptr) f32[i] = a;
     }
   }
 }
@@ -132,14 +135,16 @@ cudaError_t launch_wait_timeout_selftest(unsigned int* err, uint64_t limit_ns, u
 }
 
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice, void* dk,
-                                 void* dv, const PromptMap& map, int row_elems, cudaStream_t stream) {
+                                 void* dv, float* f32_k, float* f32_v, const PromptMap& map, int row_elems,
+                                 cudaStream_t stream) {
   if (map.ngroups == 0) return cudaSuccess;
   const int row4 = row_elems / 4;
   const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
   if (n4 == 0) return cudaSuccess;
   prompt_reduce_kernel<<<grid_for(n4), 256, 0, stream>>>(
       map, reinterpret_cast<const float4*>(src_k), reinterpret_cast<const float4*>(src_v), nsplit,
-      static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv), row4);
+      static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv),
+      reinterpret_cast<float4*>(f32_k), reinterpret_cast<float4*>(f32_v), row4);
   return cudaGetLastError();
 }
 

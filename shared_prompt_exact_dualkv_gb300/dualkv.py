@@ -27,7 +27,7 @@ EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_st
             "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
             "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
-            "dualkv_packed_positions", "dualkv_selftest_wait_timeout")
+            "dualkv_packed_positions", "dualkv_selftest_wait_timeout", "dualkv_fwd_partial", "dualkv_bwd_partial")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -102,6 +102,13 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_packed_positions.restype = ctypes.c_int
     lib.dualkv_selftest_wait_timeout.argtypes = [c_i64, c_i32, c_p]
     lib.dualkv_selftest_wait_timeout.restype = ctypes.c_int
+    lib.dualkv_fwd_partial.argtypes = [c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32, c_i32, c_f, c_i64, c_i64,
+                                       c_p, c_p, c_p]
+    lib.dualkv_fwd_partial.restype = ctypes.c_int
+    lib.dualkv_bwd_partial.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, p_i32, c_i32, c_i32, c_i32, c_f,
+                                       ctypes.c_int, c_i32, c_i64, c_i64, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p,
+                                       c_p, c_p, c_p]
+    lib.dualkv_bwd_partial.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib
@@ -190,6 +197,38 @@ def dualkv_bwd_static_workspace(q, k, v, out, dout, lse, P: int, R_lens: Sequenc
                                          _stream(stream))
     if check:
         _check(st, "dualkv_bwd_static_workspace")
+    return st
+
+
+def dualkv_fwd_partial(q, k, v, P: int, R_lens: Sequence[int], prompt_rows, out, lse, softmax_scale: float,
+                       stream=None, check: bool = True) -> int:
+    """Calls dualkv_fwd_partial: the prompt query rows prompt_rows = (lo, hi)
+    and every response row."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    lo, hi = prompt_rows
+    st = lib.dualkv_fwd_partial(_ptr(q), _ptr(k), _ptr(v), int(P), len(R_lens), _lens(R_lens), Hq, Hkv, d,
+                                float(softmax_scale), int(lo), int(hi), _ptr(out), _ptr(lse), _stream(stream))
+    if check:
+        _check(st, "dualkv_fwd_partial")
+    return st
+
+
+def dualkv_bwd_partial(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], prompt_rows, softmax_scale: float,
+                       deterministic: bool, workspace, dq, dk, dv, dq_prompt=None, dk_prompt=None, dv_prompt=None,
+                       num_splits: int = 0, stream=None, check: bool = True) -> int:
+    """Calls dualkv_bwd_partial; dq_prompt [P,Hq,d] and dk_prompt/dv_prompt
+    [P,Hkv,d] are optional fp32 device tensors for the unrounded prompt rows."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    lo, hi = prompt_rows
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.dualkv_bwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P), len(R_lens),
+                                _lens(R_lens), Hq, Hkv, d, float(softmax_scale), 1 if deterministic else 0,
+                                int(num_splits), int(lo), int(hi), _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(dq_prompt), _ptr(dk_prompt), _ptr(dv_prompt), _stream(stream))
+    if check:
+        _check(st, "dualkv_bwd_partial")
     return st
 
 

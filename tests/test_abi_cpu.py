@@ -245,3 +245,29 @@ def test_static_scratch_limit_matches_header_constant(D):
                                                        0.125, 0, 0, None, None, None, None)
     assert call(hi) == D.DUALKV_ERR_WORKSPACE
     assert call(lo) != D.DUALKV_ERR_WORKSPACE
+
+
+def test_partial_entry_points_argument_errors(D):
+    """dualkv_fwd_partial / dualkv_bwd_partial refuse a prompt part that is not
+    a tile-aligned sub-range of [0, P) before anything is launched."""
+    R = _lens(64, 64)
+
+    def fwd_p(lo, hi, **kw):
+        a = dict(q=A, P=300, out=A)
+        a.update(kw)
+        return D.lib.dualkv_fwd_partial(a["q"], A, A, a["P"], 2, R, 2, 1, 64, 0.125, lo, hi, a["out"], A, None)
+
+    def bwd_p(lo, hi, **kw):
+        a = dict(dqp=None, dkp=None, dvp=None, ws_bytes=1 << 30)
+        a.update(kw)
+        return D.lib.dualkv_bwd_partial(A, A, A, A, A, A, 300, 2, R, 2, 1, 64, 0.125, 0, 0, lo, hi, A, a["ws_bytes"],
+                                        A, A, A, a["dqp"], a["dkp"], a["dvp"], None)
+
+    for lo, hi in ((64, 128), (0, 200), (128, 0), (-128, 128), (0, 301), (301, 301), (256, 384)):
+        assert fwd_p(lo, hi) == D.DUALKV_ERR_INVALID_ARG, (lo, hi)
+        assert bwd_p(lo, hi) == D.DUALKV_ERR_INVALID_ARG, (lo, hi)
+    assert fwd_p(0, 128, q=None) == D.DUALKV_ERR_INVALID_ARG
+    assert fwd_p(0, 128, out=A + 8) == D.DUALKV_ERR_ALIGNMENT
+    assert bwd_p(0, 300, dqp=A + 4) == D.DUALKV_ERR_ALIGNMENT
+    assert bwd_p(0, 300, dvp=A + 8) == D.DUALKV_ERR_ALIGNMENT
+    assert bwd_p(0, 300, ws_bytes=16) == D.DUALKV_ERR_WORKSPACE
