@@ -67,7 +67,9 @@ typedef enum {
   DUALKV_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned */
   DUALKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
   DUALKV_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
-  DUALKV_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by dualkv_last_device_error) */
+  DUALKV_ERR_TIMEOUT = 6,      /* a device-side wait gave up (reported by dualkv_last_device_error) */
+  DUALKV_ERR_CHECK = 7         /* checks build only: a device-side index or pipeline check failed
+                                  (reported by dualkv_last_device_error) */
 } dualkv_status;
 
 /*
@@ -250,7 +252,8 @@ DUALKV_API const char* dualkv_status_string(int status);
 /*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns DUALKV_OK, DUALKV_ERR_TIMEOUT (a bounded device wait gave
- * up; *site, if non-NULL, receives the kernel-specific wait site id) or
+ * up; *site, if non-NULL, receives the kernel-specific wait site id),
+ * DUALKV_ERR_CHECK (checks build: a device-side check failed at *site) or
  * DUALKV_ERR_CUDA if the synchronisation itself failed.
  */
 DUALKV_API int dualkv_last_device_error(void* stream, int32_t* site);
@@ -273,6 +276,20 @@ DUALKV_API int dualkv_trace_read(double* ms, int64_t* launches, int32_t n);
 
 /* Library version as major*10000 + minor*100 + patch. */
 DUALKV_API int dualkv_version(void);
+
+/*
+ * 1 if this library is the checks build (compiled with DUALKV_CHECKS), else
+ * 0.  No counterpart on the DualKV pages: a debugging aid.  In the checks
+ * build every kernel tests, before each global access and each tile-copy
+ * coordinate it computes, that the index lies inside its buffer, and at the
+ * end of each CTA that its pipeline roles (copy producer, MMA issuer,
+ * elementwise warps) completed the same number of steps as the schedule
+ * gave them.  A failed check never traps: the access is skipped and the
+ * first failure's site is recorded in the device error word, which
+ * dualkv_last_device_error() returns as DUALKV_ERR_CHECK.  Results are those
+ * of the regular build whenever no check fails.
+ */
+DUALKV_API int dualkv_checks_enabled(void);
 
 #ifdef __cplusplus
 }

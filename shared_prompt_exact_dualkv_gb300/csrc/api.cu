@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "../../include/dualkv.h"
+#include "checks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -446,7 +447,8 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
     });
   if (e == cudaSuccess && map->ngroups > 0) {
     TraceScope ts(3, cs);
-    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, f32.dk, f32.dv, *map, sh.Hkv * sh.d, cs);
+    e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, f32.dk, f32.dv, *map, sh.Hkv * sh.d, err,
+                             cs);
   }
   if (e == cudaSuccess)
     e = launch_chunks(sq.get(), q_items, [&](const Sched& c) {
@@ -465,6 +467,8 @@ extern "C" {
 
 int dualkv_version(void) { return 100; }
 
+int dualkv_checks_enabled(void) { return kChecks ? 1 : 0; }
+
 const char* dualkv_status_string(int status) {
   switch (status) {
     case DUALKV_OK: return "ok";
@@ -474,6 +478,7 @@ const char* dualkv_status_string(int status) {
     case DUALKV_ERR_WORKSPACE: return "workspace missing or too small";
     case DUALKV_ERR_CUDA: return "CUDA runtime or launch error";
     case DUALKV_ERR_TIMEOUT: return "device-side wait timed out";
+    case DUALKV_ERR_CHECK: return "device-side check failed (checks build)";
     default: return "unknown status";
   }
 }
@@ -620,7 +625,8 @@ int dualkv_last_device_error(void* stream, int32_t* site) {
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return DUALKV_ERR_CUDA;
   if (site) *site = static_cast<int32_t>(w >> 8);
-  return static_cast<int>(w & 0xFFu) == DUALKV_ERR_TIMEOUT ? DUALKV_ERR_TIMEOUT : DUALKV_ERR_CUDA;
+  const int kind = static_cast<int>(w & 0xFFu);
+  return (kind == DUALKV_ERR_TIMEOUT || kind == DUALKV_ERR_CHECK) ? kind : DUALKV_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ fixed scratch

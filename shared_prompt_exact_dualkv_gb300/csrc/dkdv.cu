@@ -28,6 +28,7 @@
 // the two halves never touch each other's unread columns.
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 128);
+  const RoleSteps steps{reinterpret_cast<int32_t*>(sm + L::kBar + 160)};  // checks build only
   float* vec = reinterpret_cast<float*>(sm + L::kVec);
 
   const int warp = threadIdx.x >> 5;
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bar[kdSReady], kEwThreads);
     mbar_init(&bar[kAccDone], 1);
     fence_mbar_init();
+    steps.init();
     tma_prefetch_desc(&mQ);
     tma_prefetch_desc(&mK);
     tma_prefetch_desc(&mV);
@@ -210,6 +213,8 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (n > 0) {
+      // (an out-of-range tile copy would only read zeros; the checks record it)
+      check(R.k0 >= 0 && R.k0 < s.T && hk < s.Hkv, err, 1101);
       if (elect_one()) {
         mbar_arrive_expect_tx(&bar[kKVFull], 2 * L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) {
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(320, 1)
           const int q = t.q0() + lane * 4 + u;
           l2[u] = INFINITY;
           dd[u] = 0.f;
-          if (q < t.seg_end) {
+          if (q < t.seg_end && check_index(static_cast<int64_t>(h) * s.T + q, static_cast<int64_t>(s.Hq) * s.T, err, 1103)) {
             l2[u] = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
             dd[u] = Dvec[static_cast<size_t>(h) * s.T + q];
           }
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < n; ++i) {
         const int st = i & 1;
         if (i >= 2 && !mbar_wait(&bar[kQEmpty + st], ((i >> 1) - 1) & 1, err, 701)) break;
+        check(it.q0() >= 0 && it.q0() < s.T && it.head(R) < s.Hq, err, 1102);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kQFull + st], 2 * L::kTileBytes);
           for (int a = 0; a < D / 64; ++a) {
@@ -249,6 +255,7 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         issued = i + 1;
+        if (lane == 0) steps.put(0, issued);
         float* vl = vec + st * 256;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -328,6 +335,7 @@ __global__ void __launch_bounds__(320, 1)
                  (i > 0 || kk > 0) ? 1u : 0u);
         if (elect_one()) mma_commit(&bar[kQEmpty + st]);
         if (i + 1 < n) issue_dp(i + 1);
+        if (lane == 0) steps.put(1, i + 1);
       }
       if (elect_one()) mma_commit(&bar[kAccDone]);
     }
@@ -404,6 +412,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar[kdSReady]);
+        if (row == 0) steps.put(2 + half, i + 1);
       }
     }
     // ---------------------------------------------------------------- epilogue
@@ -420,6 +429,7 @@ __global__ void __launch_bounds__(320, 1)
       const size_t slice = static_cast<size_t>(s.acc_rows) * s.Hkv * D;
       float* pk_out = acc_k + (deterministic ? R.split * slice : 0) + base;
       float* pv_out = acc_v + (deterministic ? R.split * slice : 0) + base;
+      const bool in_acc = !valid || check(R.acc0 + row < s.acc_rows && R.split < s.num_splits && hk < s.Hkv, err, 1104);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which ? kColdK : kColdV) + half * (D / 2);
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int u = 0; u < 32; ++u) r[u] = 0u;
           }
-          if (valid && (ok || n == 0)) {
+          if (valid && in_acc && (ok || n == 0)) {
 #pragma unroll
             for (int u = 0; u < 32; u += 4) {
               const float a0 = __uint_as_float(r[u]) * mul, a1 = __uint_as_float(r[u + 1]) * mul;
@@ -464,7 +474,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int u = 0; u < 16; ++u)
             pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
-          if (valid) {
+          if (valid && check(k >= 0 && k < s.T && hk < s.Hkv, err, 1105)) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -476,6 +486,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 256) steps.verify(n, err, 1106);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();

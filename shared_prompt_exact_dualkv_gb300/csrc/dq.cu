@@ -17,6 +17,7 @@
 // column) double buffer [384,448) and [448,512).
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 192);
+  const RoleSteps steps{reinterpret_cast<int32_t*>(sm + L::kBar + 200)};  // checks build only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar[kdSFree + i], 1);
     }
     fence_mbar_init();
+    steps.init();
     tma_prefetch_desc(&mQ);
     tma_prefetch_desc(&mK);
     tma_prefetch_desc(&mV);
@@ -114,6 +117,8 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- producer
     // The warp runs the loop converged; one elected lane issues each copy.
     {
+      // (an out-of-range tile copy would only read zeros; the checks record it)
+      check(w.q0 >= 0 && w.q0 < s.T && h < s.Hq, err, 1201);
       if (elect_one()) {
         mbar_arrive_expect_tx(&bar[kQFull], 2 * L::kTileBytes);
         for (int a = 0; a < D / 64; ++a) {
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(320, 1)
       int ks = 0, kph = 0, vs = 0, vph = 0, k_issued = 0, v_issued = 0;
       for (int j = 0; j < n; ++j) {
         const int k0 = w.k0(j);
+        check(k0 >= 0 && k0 < s.T && hk < s.Hkv, err, 1202);
         if (j >= L::kKStages && !mbar_wait(&bar[kKEmpty + ks], kph ^ 1, err, 401)) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
@@ -141,6 +147,7 @@ __global__ void __launch_bounds__(320, 1)
         if (++ks == L::kKStages) { ks = 0; kph ^= 1; }
         if (++vs == L::kVStages) { vs = 0; vph ^= 1; }
       }
+      if (lane == 0) steps.put(0, v_issued);
       // Before the CTA can exit, every copy this warp issued must have landed
       // (the consumers may have stopped early on an error).
       for (int j = (k_issued > L::kKStages ? k_issued - L::kKStages : 0); j < k_issued; ++j)
@@ -204,6 +211,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (elect_one()) mma_commit(&bar[kdSFree + b]);
         if (elect_one()) mma_commit(&bar[kKEmpty + ks]);
+        if (lane == 0) steps.put(1, j + 1);
       }
     }
   } else {
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(320, 1)
     const int q = w.q0 + row;
     // Rows past the segment end are never stored; give them P = 0.
     float lse2 = INFINITY, Dr = 0.f;
-    if (q < w.q_end) {
+    if (q < w.q_end && check_index(static_cast<int64_t>(h) * s.T + q, static_cast<int64_t>(s.Hq) * s.T, err, 1203)) {
       lse2 = lse[static_cast<size_t>(h) * s.T + q] * 1.4426950408889634f;
       Dr = Dvec[static_cast<size_t>(h) * s.T + q];
     }
@@ -276,6 +284,7 @@ __global__ void __launch_bounds__(320, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[kdSFull + b]);
+      if (row == 0) steps.put(2 + half, j + 1);
     }
     // ---------------------------------------------------------------- epilogue
     const int bl = (n - 1) & 1;
@@ -288,7 +297,8 @@ __global__ void __launch_bounds__(320, 1)
       // [prompt rows of all groups, Hq, D]) when the caller asked for it.
       const int32_t seg = static_cast<int32_t>(item_seg(item));
       float4* dst32 = nullptr;
-      if (dq_prompt != nullptr && s.prompt_of(seg) == seg)
+      if (dq_prompt != nullptr && s.prompt_of(seg) == seg &&
+          (!valid || check(s.acc_row[seg] + (q - s.off[seg]) < s.acc_rows, err, 1205)))
         dst32 = reinterpret_cast<float4*>(
             dq_prompt + (static_cast<size_t>(s.acc_row[seg] + (q - s.off[seg])) * s.Hq + h) * D + half * (D / 2));
 #pragma unroll
@@ -300,7 +310,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * s.scale, __uint_as_float(r[2 * i + 1]) * s.scale);
-        if (valid) {
+        if (valid && check(q >= 0 && q < s.T && h < s.Hq, err, 1204)) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           if (dst32 != nullptr) {
@@ -316,6 +326,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 256) steps.verify(n, err, 1206);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();

@@ -26,6 +26,7 @@
 // the PV product that reads P.
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 192);
+  const RoleSteps steps{reinterpret_cast<int32_t*>(sm + L::kBar + 200)};  // checks build only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar[kODone + i], 1);
     }
     fence_mbar_init();
+    steps.init();
     tma_prefetch_desc(&mQ);
     tma_prefetch_desc(&mK);
     tma_prefetch_desc(&mV);
@@ -193,6 +196,8 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
+    // (an out-of-range tile copy would only read zeros; the checks record it)
+    check(w.q0 >= 0 && w.q0 < s.T && h0 + nheads <= s.Hq, err, 1001);
     if (elect_one()) {
       mbar_arrive_expect_tx(&bar[kQFull], nheads * L::kTileBytes);
       for (int x = 0; x < nheads; ++x)
@@ -205,6 +210,7 @@ __global__ void __launch_bounds__(320, 1)
       const int k0 = w.k0(j);
       uint8_t* sK = sm + L::kK + ks * L::kTileBytes;
       uint8_t* sV = sm + L::kV + vs * L::kTileBytes;
+      check(k0 >= 0 && k0 < s.T && hk < s.Hkv, err, 1002);
       if (j >= L::kKS && !mbar_wait(&bar[kKEmpty + ks], ((j / L::kKS) - 1) & 1, err, 101)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bar[kKFull + ks], L::kTileBytes);
@@ -218,6 +224,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       v_issued = j + 1;
     }
+    if (lane == 0) steps.put(0, v_issued);
     // Before the CTA can exit, every copy this warp issued must have landed
     // (the consumers may have stopped early on an error).
     for (int j = (k_issued > L::kKS ? k_issued - L::kKS : 0); j < k_issued; ++j)
@@ -248,6 +255,7 @@ __global__ void __launch_bounds__(320, 1)
       return true;
     };
     for (int x = 0; ok && x < nheads; ++x) ok = issue_s(0, x);
+    int done = 0;
     for (int j = 0; ok && j < n; ++j) {
       const int vs = j % L::kVS;
       const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
@@ -268,7 +276,9 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit(&bar[kODone + x]);
         }
       }
+      if (ok) done = j + 1;
     }
+    if (lane == 0) steps.put(1, done);
   } else if (warp / 4 < nheads) {
     // ---------------------------------------------------------------- softmax
     const int x = warp >> 2;  // head of this warpgroup
@@ -316,6 +326,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();  // every lane's P (and rescaled O) is stored and fenced
       if (lane == 0) mbar_arrive(&bar[kPFull + x]);
+      if (row == 0) steps.put(2 + x, j + 1);
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bar[kODone + x], 0, err, 303);
@@ -334,17 +345,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-        if (valid) {
+        if (valid && check(q >= 0 && q < s.T && h < s.Hq, err, 1003)) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (valid) lse[static_cast<size_t>(h) * s.T + q] = (m_use + log2f(l)) * 0.6931471805599453f;
+      if (valid && check(q >= 0 && q < s.T && h < s.Hq, err, 1003))
+        lse[static_cast<size_t>(h) * s.T + q] = (m_use + log2f(l)) * 0.6931471805599453f;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 256) steps.verify(n, err, 1004);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();

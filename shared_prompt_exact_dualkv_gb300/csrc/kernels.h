@@ -49,7 +49,7 @@ struct PromptMap {
 // row order ([prompt rows of all groups, Hkv, d]).
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
                                  void* dk, void* dv, float* f32_k, float* f32_v, const PromptMap& map,
-                                 int row_elems, cudaStream_t stream);
+                                 int row_elems, unsigned int* err, cudaStream_t stream);
 
 // Self-test of the bounded waits: a wait on an mbarrier phase that never
 // completes gives up after limit_ns and records a timeout at `site`.

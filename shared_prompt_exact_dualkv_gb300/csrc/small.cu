@@ -3,6 +3,7 @@
 // research-map page) and the prompt dK/dV reduction + bf16 cast.
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
                                                             const float4* __restrict__ src_v, int nsplit,
                                                             int64_t slice4, uint2* __restrict__ dk,
                                                             uint2* __restrict__ dv, float4* __restrict__ f32_k,
-                                                            float4* __restrict__ f32_v, int row4) {
+                                                            float4* __restrict__ f32_v, int row4,
+                                                            unsigned int* err) {
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
   const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
@@ -64,6 +66,7 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
       const int mid = (lo + hi + 1) >> 1;
       if (map.acc_row[mid] <= r) lo = mid; else hi = mid - 1;
     }
+    if (!check(r >= map.acc_row[lo] && r < map.acc_row[lo + 1], err, 1301)) continue;
     const int64_t out = (int64_t(map.packed_row[lo]) + (r - map.acc_row[lo])) * row4 + (i - int64_t(r) * row4);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
@@ -136,7 +139,7 @@ cudaError_t launch_wait_timeout_selftest(unsigned int* err, uint64_t limit_ns, u
 
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice, void* dk,
                                  void* dv, float* f32_k, float* f32_v, const PromptMap& map, int row_elems,
-                                 cudaStream_t stream) {
+                                 unsigned int* err, cudaStream_t stream) {
   if (map.ngroups == 0) return cudaSuccess;
   const int row4 = row_elems / 4;
   const int64_t n4 = int64_t(map.acc_row[map.ngroups]) * row4;
@@ -144,7 +147,7 @@ cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsp
   prompt_reduce_kernel<<<grid_for(n4), 256, 0, stream>>>(
       map, reinterpret_cast<const float4*>(src_k), reinterpret_cast<const float4*>(src_v), nsplit,
       static_cast<int64_t>(slice / 4), static_cast<uint2*>(dk), static_cast<uint2*>(dv),
-      reinterpret_cast<float4*>(f32_k), reinterpret_cast<float4*>(f32_v), row4);
+      reinterpret_cast<float4*>(f32_k), reinterpret_cast<float4*>(f32_v), row4, err);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,10 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdualkv.so")
+# DUALKV_LIBRARY=checks loads the checks build (libdualkv_checks.so, made by
+# build.build(checks=True)) instead of the regular library.
+LIB_PATH = os.path.join(_HERE, "libdualkv_checks.so" if os.environ.get("DUALKV_LIBRARY") == "checks"
+                        else "libdualkv.so")
 
 DUALKV_OK = 0
 DUALKV_ERR_INVALID_ARG = 1
@@ -22,12 +25,14 @@ DUALKV_ERR_ALIGNMENT = 3
 DUALKV_ERR_WORKSPACE = 4
 DUALKV_ERR_CUDA = 5
 DUALKV_ERR_TIMEOUT = 6
+DUALKV_ERR_CHECK = 7
 
 EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_status_string",
             "dualkv_last_device_error", "dualkv_trace_enable", "dualkv_trace_read", "dualkv_version",
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
             "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
-            "dualkv_packed_positions", "dualkv_selftest_wait_timeout", "dualkv_fwd_partial", "dualkv_bwd_partial")
+            "dualkv_packed_positions", "dualkv_selftest_wait_timeout", "dualkv_fwd_partial", "dualkv_bwd_partial",
+            "dualkv_checks_enabled")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -109,6 +114,8 @@ def _load() -> ctypes.CDLL:
                                        ctypes.c_int, c_i32, c_i64, c_i64, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p,
                                        c_p, c_p, c_p]
     lib.dualkv_bwd_partial.restype = ctypes.c_int
+    lib.dualkv_checks_enabled.argtypes = []
+    lib.dualkv_checks_enabled.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
     lib.dualkv_version.restype = ctypes.c_int
     return lib

@@ -271,3 +271,18 @@ def test_partial_entry_points_argument_errors(D):
     assert bwd_p(0, 300, dqp=A + 4) == D.DUALKV_ERR_ALIGNMENT
     assert bwd_p(0, 300, dvp=A + 8) == D.DUALKV_ERR_ALIGNMENT
     assert bwd_p(0, 300, ws_bytes=16) == D.DUALKV_ERR_WORKSPACE
+
+
+def test_checks_build_compiles_and_reports_itself(D):
+    """The checks build links with the same exports; only it reports
+    dualkv_checks_enabled() == 1 (loaded in a child process)."""
+    import subprocess
+    import sys
+    from shared_prompt_exact_dualkv_gb300 import build
+    build.build(checks=True)
+    code = ("from shared_prompt_exact_dualkv_gb300 import dualkv as D; "
+            "print(D.lib.dualkv_checks_enabled(), all(hasattr(D.lib, n) for n in D.EXPORTED))")
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, DUALKV_LIBRARY="checks"), cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.stdout.split() == ["1", "True"], r.stdout + r.stderr
+    assert D.lib.dualkv_checks_enabled() == 0
