@@ -382,6 +382,66 @@ def layer_leg(D, w, dev, stream):
     return out
 
 
+def gemm_leg(D, dev, stream, rows: int):
+    """The layer's tensor-core GEMM (dualkv_gemm) against cuBLAS (torch.matmul,
+    bf16 in, fp32 accumulation) on the same bf16 inputs, for one shape of each
+    operand layout of a Qwen3-8B layer on `rows` packed rows: the QKV
+    projection (X.W^T), the gate/up input gradient (dY.W) and the gate/up
+    weight gradient (dY^T.X, fp32 out)."""
+    H, I, nqkv = 4096, 12288, 6144
+    gen = torch.Generator(device=dev).manual_seed(3)
+    rnd = lambda *shape: torch.randn(shape, device=dev, generator=gen).to(torch.bfloat16)
+    cases = {
+        "qkv_fwd x.wT": (0, rnd(rows, H), rnd(nqkv, H), (rows, nqkv), torch.bfloat16),
+        "gate_up_dx dy.w": (1, rnd(rows, 2 * I), rnd(2 * I, H), (rows, H), torch.bfloat16),
+        "gate_up_dw dyT.x": (2, rnd(rows, 2 * I), rnd(rows, H), (2 * I, H), torch.float32),
+    }
+    out = {}
+    for name, (kind, A, B, yshape, ydt) in cases.items():
+        Y = torch.empty(yshape, dtype=ydt, device=dev)
+        # cuBLAS arm: the same product in bf16 (for kind 2 with a bf16 result,
+        # which it writes in half the bytes of the library's fp32 one)
+        if kind == 0:
+            M, K, N = A.shape[0], A.shape[1], B.shape[0]
+            cublas = lambda: torch.matmul(A, B.T)
+        elif kind == 1:
+            M, K, N = A.shape[0], A.shape[1], B.shape[1]
+            cublas = lambda: torch.matmul(A, B)
+        else:
+            K, M, N = A.shape[0], A.shape[1], B.shape[1]
+            cublas = lambda: torch.matmul(A.T, B)
+        ours = lambda: D.dualkv_gemm(kind, A, B, Y, stream=stream)
+        flops = 2.0 * M * N * K
+        res = {"M": M, "N": N, "K": K}
+        for who, fn in (("library", ours), ("cublas", cublas)):
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(5):
+                    fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / 5
+            res[who] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+        res["library_over_cublas"] = res["library"]["tflops"] / res["cublas"]["tflops"]
+        with torch.cuda.stream(stream):
+            ours()
+            check = cublas().float()
+        torch.cuda.synchronize()
+        res["rel_l2_vs_cublas"] = float((Y.float() - check).norm() / check.norm())
+        del check
+        out[name] = res
+        del Y
+    st, site = D.dualkv_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error {st} at wait site {site}")
+    return out
+
+
 def groups_leg(D, dev, stream):
     """Four prompt groups (Qwen3-8B shapes: 32/8 heads, d 128; each group a
     4096-token prompt and 8 responses of 4096 tokens) as one grouped forward +
@@ -744,6 +804,7 @@ def main():
         del q, k, v, do, out, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
         result["layer"] = layer_leg(D, w, dev, stream)
+        result["layer"]["gemm"] = gemm_leg(D, dev, stream, w.T)
 
     if rank == 0:
         print(json.dumps(result), flush=True)

@@ -88,11 +88,27 @@ DUALKV_API int dualkv_fwd(const void* q, const void* k, const void* v, int64_t P
                void* out, float* lse, void* stream);
 
 /*
- * Workspace bytes that dualkv_bwd needs for this shape and reduction mode
- * (0 = fp32 atomics into one prompt accumulator, 1 = deterministic per-split
- * partials reduced in a fixed order).  num_splits is the number of sequence
- * chunks a prompt key tile's work is divided into (0 = library choice).
- * Returns 0 for arguments dualkv_bwd would reject.
+ * Backward modes: the `deterministic` argument of the backward calls.
+ *   DUALKV_BWD_ATOMIC (0): the prompt's dK/dV are summed over the sequences
+ *     with fp32 atomics (research-map page, "Approach"), and dQ is computed in
+ *     the same kernel as dK/dV, each key tile adding its share of dQ with fp32
+ *     atomics; the workspace then also holds an fp32 dQ accumulator of
+ *     T*Hq*d*4 bytes.  Results vary in the last bits from run to run.
+ *   DUALKV_BWD_DETERMINISTIC (1): per-split fp32 partials summed in a fixed
+ *     order, and dQ from a separate kernel with one writer per row; bitwise
+ *     reproducible.
+ *   DUALKV_BWD_ATOMIC_SPLIT_DQ (2): prompt dK/dV with fp32 atomics, dQ from
+ *     the separate kernel (the smallest workspace).
+ */
+#define DUALKV_BWD_ATOMIC 0
+#define DUALKV_BWD_DETERMINISTIC 1
+#define DUALKV_BWD_ATOMIC_SPLIT_DQ 2
+
+/*
+ * Workspace bytes that dualkv_bwd needs for this shape and backward mode
+ * (DUALKV_BWD_*).  num_splits is the number of sequence chunks a prompt key
+ * tile's work is divided into (0 = library choice).  Returns 0 for arguments
+ * dualkv_bwd would reject (including an unknown mode).
  */
 DUALKV_API size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq,
                                   int32_t Hkv, int32_t d, int deterministic, int32_t num_splits);
@@ -104,9 +120,10 @@ DUALKV_API size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t
  *                       as dualkv_fwd wrote them).
  *   dout              : device [T, Hq, d] bf16 output gradient (prompt rows
  *                       carry the summed gradient of the shared rows).
- *   deterministic     : 0 = prompt dK/dV summed with fp32 atomics;
- *                       1 = per-split fp32 partials summed in a fixed order
- *                       (bitwise reproducible).
+ *   deterministic     : the backward mode, DUALKV_BWD_ATOMIC (0),
+ *                       DUALKV_BWD_DETERMINISTIC (1, bitwise reproducible) or
+ *                       DUALKV_BWD_ATOMIC_SPLIT_DQ (2); other values are
+ *                       DUALKV_ERR_INVALID_ARG.
  *   num_splits        : sequence chunks per prompt key tile (0 = library
  *                       choice; must match the value given to
  *                       dualkv_bwd_workspace_bytes).

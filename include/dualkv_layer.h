@@ -37,14 +37,14 @@
  * Accepted shapes: d in {64, 128}; Hq % Hkv == 0; hidden % 8 == 0 and
  * hidden <= 6144; inter % 8 == 0; the group rules of dualkv_fwd_groups.
  *
- * The GEMMs are plain cuBLAS calls (bf16 inputs, fp32 accumulation) on the
- * caller's stream; RMSNorm, RoPE, SwiGLU and attention are this library's
- * kernels.  cuBLAS uses a slice of the caller's workspace as its scratch.  Its
- * handle (one per host thread and device, created on first use and kept) is
- * the only allocation made inside the library.
+ * Every step runs in this library's kernels on the caller's stream: the
+ * GEMMs on the tcgen05 tensor cores (bf16 inputs, fp32 accumulation, bf16
+ * activations and fp32 weight gradients), RMSNorm, RoPE, SwiGLU and the
+ * attention.  The library allocates no device memory.
  *
  * Errors: the status codes of dualkv.h.  Arguments are checked before
- * anything is launched; a cuBLAS failure maps to DUALKV_ERR_CUDA.
+ * anything is launched; a launch failure maps to DUALKV_ERR_CUDA, and a
+ * bounded device wait that gives up is reported by dualkv_last_device_error().
  */
 #ifndef DUALKV_LAYER_H_
 #define DUALKV_LAYER_H_
@@ -87,8 +87,8 @@ typedef struct {
 
 /*
  * Bytes of device workspace for one forward + backward of this shape: the
- * activations the forward saves for the backward, the backward's scratch and
- * cuBLAS's scratch.  Returns 0 for arguments the layer calls would reject.
+ * activations the forward saves for the backward and the backward's scratch.
+ * Returns 0 for arguments the layer calls would reject.
  */
 DUALKV_API size_t dualkv_layer_workspace_bytes(const dualkv_layer_config* cfg, int32_t G, const int64_t* P,
                                                const int32_t* N, const int32_t* R_lens);
@@ -122,6 +122,22 @@ DUALKV_API int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_lay
  */
 DUALKV_API int dualkv_packed_positions(int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens,
                                        int32_t* pos, int64_t capacity);
+
+/*
+ * One of the layer's GEMMs on its own (no counterpart on the DualKV pages;
+ * exposed so that tests and benchmarks can check and time the tensor-core
+ * GEMM the layer runs).  Row-major bf16 operands, fp32 accumulation:
+ *   kind 0: Y[M,N] = A[M,K] . B[N,K]^T, bf16 Y; accumulate != 0 adds the
+ *           result to what Y holds (Y = Y + A.B^T, one rounding);
+ *   kind 1: Y[M,N] = A[M,K] . B[K,N], bf16 Y;
+ *   kind 2: Y[M,N] = A[K,M]^T . B[K,N], fp32 Y (zeros when K == 0).
+ * Every row length of A, B and Y (the contiguous dimension) must be a
+ * multiple of 8, and every pointer 16-byte aligned.  M, N, K >= 0 and below
+ * 2^31.  Returns DUALKV_OK, DUALKV_ERR_INVALID_ARG, DUALKV_ERR_UNSUPPORTED
+ * (a row length not a multiple of 8), DUALKV_ERR_ALIGNMENT or DUALKV_ERR_CUDA.
+ */
+DUALKV_API int dualkv_gemm(int32_t kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* Y,
+                           int32_t accumulate, void* stream);
 
 #ifdef __cplusplus
 }

@@ -21,8 +21,8 @@ LIB_PATH = os.path.join(HERE, "libdualkv.so")
 CHECKS_BUILD_DIR = os.path.join(HERE, "_build_checks")
 CHECKS_LIB_PATH = os.path.join(HERE, "libdualkv_checks.so")
 
-SOURCES = ["api.cu", "fwd.cu", "dq.cu", "dkdv.cu", "small.cu", "layer_kernels.cu", "layer_api.cu"]
-LIBS = ["-lcublas"]
+SOURCES = ["api.cu", "fwd.cu", "dq.cu", "dkdv.cu", "small.cu", "layer_kernels.cu", "layer_api.cu", "gemm.cu"]
+LIBS = []
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -241,22 +241,33 @@ int resolve_splits(const Shape& sh, int32_t num_splits) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Backward modes (the `deterministic` argument of the ABI).
+constexpr int kModeAtomic = DUALKV_BWD_ATOMIC;              // fp32 atomics, dQ fused into the dK/dV kernel
+constexpr int kModeDeterministic = DUALKV_BWD_DETERMINISTIC;
+constexpr int kModeSplitDq = DUALKV_BWD_ATOMIC_SPLIT_DQ;    // fp32 atomics for prompt dK/dV, separate dQ kernel
+
+bool mode_ok(int mode) { return mode == kModeAtomic || mode == kModeDeterministic || mode == kModeSplitDq; }
+
 struct WsLayout {
-  size_t D = 0, acc_k = 0, acc_v = 0, total = 0;
+  size_t D = 0, acc_k = 0, acc_v = 0, dq_acc = 0, total = 0;
   size_t acc_floats = 0;  // floats in one of acc_k / acc_v
   size_t slice = 0;       // floats per split slice
   int S = 1;
 };
 
-WsLayout workspace_layout(const Shape& sh, int deterministic, int S) {
+// D [Hq, T]; the prompt accumulators (one slice, or S in deterministic mode);
+// in the fused mode the dQ accumulator [Hq][d/4][T][4] follows them, so that
+// one zero-fill covers everything the atomics add into.
+WsLayout workspace_layout(const Shape& sh, int mode, int S) {
   WsLayout w;
   w.S = S;
   w.slice = size_t(sh.total_P) * sh.Hkv * sh.d;
-  w.acc_floats = deterministic ? w.slice * S : w.slice;
+  w.acc_floats = mode == kModeDeterministic ? w.slice * S : w.slice;
   w.D = 0;
   w.acc_k = align256(size_t(sh.T) * sh.Hq * 4);
   w.acc_v = w.acc_k + align256(w.acc_floats * 4);
-  w.total = w.acc_v + align256(w.acc_floats * 4);
+  w.dq_acc = w.acc_v + align256(w.acc_floats * 4);
+  w.total = w.dq_acc + (mode == kModeAtomic ? align256(size_t(sh.T) * sh.Hq * sh.d * 4) : 0);
   return w;
 }
 
@@ -405,9 +416,12 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(f32.dq) ||
       !aligned16(f32.dk) || !aligned16(f32.dv))
     return DUALKV_ERR_ALIGNMENT;
-  const int det = deterministic ? 1 : 0;
+  const int mode = deterministic;
+  if (!mode_ok(mode)) return DUALKV_ERR_INVALID_ARG;
+  const int det = mode == kModeDeterministic ? 1 : 0;
+  const bool fused = mode == kModeAtomic;
   const int S = resolve_splits(sh, num_splits);
-  const WsLayout ws = workspace_layout(sh, det, S);
+  const WsLayout ws = workspace_layout(sh, mode, S);
   if (!workspace || workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DUALKV_ERR_ALIGNMENT;
 
@@ -431,6 +445,7 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   float* Dvec = reinterpret_cast<float*>(wb + ws.D);
   float* acc_k = reinterpret_cast<float*>(wb + ws.acc_k);
   float* acc_v = reinterpret_cast<float*>(wb + ws.acc_v);
+  float* dq_acc = fused ? reinterpret_cast<float*>(wb + ws.dq_acc) : nullptr;
 
   cudaError_t e;
   {
@@ -443,22 +458,34 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   if (e == cudaSuccess)
     e = launch_chunks(sk.get(), k_items, [&](const Sched& c) {
       TraceScope ts(2, cs);
-      return launch_dkdv(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, det, err, cs);
+      return launch_dkdv(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, dq_acc, det, err, cs);
     });
   if (e == cudaSuccess && map->ngroups > 0) {
     TraceScope ts(3, cs);
     e = launch_prompt_reduce(acc_k, acc_v, det ? S : 1, ws.slice, dk, dv, f32.dk, f32.dv, *map, sh.Hkv * sh.d, err,
                              cs);
   }
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && fused) {
+    // dQ was summed in fp32 by the dK/dV kernel: scale and cast.  Prompt rows
+    // outside the part this call takes are left untouched (a one-group call).
+    TraceScope ts(4, cs);
+    const bool one_prompt = sh.P.size() == 1;
+    const int64_t pe = one_prompt ? sh.P[0] : 0;
+    e = launch_dq_cast(dq_acc, dq, f32.dq, sh.T, sh.Hq, sh.d, scale, pe, int64_t(part.lo) * kTile,
+                       std::min<int64_t>(int64_t(part.hi) * kTile, pe), cs);
+  } else if (e == cudaSuccess) {
     e = launch_chunks(sq.get(), q_items, [&](const Sched& c) {
       TraceScope ts(4, cs);
       return launch_dq(c, sh.d, mQ, mK, mV, mdO, lse, Dvec, dq, f32.dq, err, cs);
     });
+  }
   return map_cuda(e);
 }
 
 }  // namespace
+
+unsigned int* device_error_word() { return error_word_ptr(); }
+
 }  // namespace dkv
 
 using namespace dkv;
@@ -503,16 +530,16 @@ int dualkv_fwd_groups(const void* q, const void* k, const void* v, int32_t G, co
 size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t* R_lens, int32_t Hq, int32_t Hkv,
                                   int32_t d, int deterministic, int32_t num_splits) {
   Shape sh;
-  if (check_shape(&sh, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK) return 0;
-  return workspace_layout(sh, deterministic ? 1 : 0, resolve_splits(sh, num_splits)).total;
+  if (check_shape(&sh, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK || !mode_ok(deterministic)) return 0;
+  return workspace_layout(sh, deterministic, resolve_splits(sh, num_splits)).total;
 }
 
 size_t dualkv_bwd_groups_workspace_bytes(int32_t G, const int64_t* P, const int32_t* N, const int32_t* R_lens,
                                          int32_t Hq, int32_t Hkv, int32_t d, int deterministic,
                                          int32_t num_splits) {
   Shape sh;
-  if (check_groups(&sh, G, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK) return 0;
-  return workspace_layout(sh, deterministic ? 1 : 0, resolve_splits(sh, num_splits)).total;
+  if (check_groups(&sh, G, P, N, R_lens, Hq, Hkv, d) != DUALKV_OK || !mode_ok(deterministic)) return 0;
+  return workspace_layout(sh, deterministic, resolve_splits(sh, num_splits)).total;
 }
 
 int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,

@@ -36,7 +36,10 @@
 namespace dkv {
 namespace {
 
-template <int D>
+// FQ: the variant that also computes dQ (the dS tile then lives in shared
+// memory).  Its layout has no alignment slack: it only fits with the
+// dynamic shared memory starting 1024-byte aligned, which the kernel checks.
+template <int D, bool FQ>
 struct DkdvLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = 2;
@@ -44,9 +47,11 @@ struct DkdvLayout {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kdO = kQ + kStages * kTileBytes;
-  static constexpr int kVec = kdO + kStages * kTileBytes;  // per stage: lse2[128], D[128] floats
+  static constexpr int kdS = kdO + kStages * kTileBytes;    // FQ: dS^T [2 query halves][128 keys][128 B]
+  static constexpr int kVec = kdS + (FQ ? kTile * kTile * 2 : 0);  // per stage: lse2[128], D[128] floats
   static constexpr int kBar = kVec + kStages * 1024;
-  static constexpr int kBytes = kBar + 256 + 1024;
+  static constexpr int kSlack = FQ ? 0 : 1024;
+  static constexpr int kBytes = kBar + 256 + kSlack;
 };
 
 enum DkdvBar {
@@ -58,7 +63,9 @@ enum DkdvBar {
   kPReady = 7,
   kdSReady = 8,
   kAccDone = 9,
-  kNumDkdvBars = 10
+  kdQFull = 10,  // FQ: this tile's dQ product is in TMEM (over the dP^T columns)
+  kdQFree = 11,  // FQ: the elementwise warps have read it out
+  kNumDkdvBars = 12
 };
 
 constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
@@ -160,16 +167,29 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-template <int D>
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// dq_acc (FQ only): fp32 dQ accumulator [Hq][D/4][T][4] (unscaled); each
+// tile's dQ = dS K is added to it with fp32 vector reductions.
+template <int D, bool FQ>
 __global__ void __launch_bounds__(320, 1)
     dkdv_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
                 const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                float* __restrict__ acc_k, float* __restrict__ acc_v, int deterministic, unsigned int* err) {
-  using L = DkdvLayout<D>;
+                float* __restrict__ acc_k, float* __restrict__ acc_v, float* __restrict__ dq_acc, int deterministic,
+                unsigned int* err) {
+  using L = DkdvLayout<D, FQ>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = FQ ? smem_raw
+                  : reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (FQ && (smem_u32(smem_raw) & 1023u) != 0) {
+    // the layout needs a 1024-byte aligned base (every thread takes this exit)
+    if (threadIdx.x == 0) record_error(err, kDevErrCheck, 1107);
+    return;
+  }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kBar + 128);
   const RoleSteps steps{reinterpret_cast<int32_t*>(sm + L::kBar + 160)};  // checks build only
@@ -198,6 +218,8 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bar[kPReady], kEwThreads);
     mbar_init(&bar[kdSReady], kEwThreads);
     mbar_init(&bar[kAccDone], 1);
+    mbar_init(&bar[kdQFull], 1);
+    mbar_init(&bar[kdQFree], kEwThreads);
     fence_mbar_init();
     steps.init();
     tma_prefetch_desc(&mQ);
@@ -325,16 +347,42 @@ __global__ void __launch_bounds__(320, 1)
                  (i > 0 || kk > 0) ? 1u : 0u);
         // the next S^T may overwrite P^T: it is issued after the dV product
         if (i + 1 < n && !issue_s(i + 1)) break;
-        // dK += dS^T Q  (dS^T read from TMEM columns [128,160) and [192,224))
         if (!mbar_wait(&bar[kdSReady], i & 1, err, 804)) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(sm + L::kQ + st * L::kTileBytes);
+        if (!FQ) {
+          // dK += dS^T Q  (dS^T read from TMEM columns [128,160) and [192,224))
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          if (elect_one()) mma_ts(tmem + kColdK, tmem + kColdP + split_col(kk), desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        if (elect_one()) mma_commit(&bar[kQEmpty + st]);
-        if (i + 1 < n) issue_dp(i + 1);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            if (elect_one()) mma_ts(tmem + kColdK, tmem + kColdP + split_col(kk), desc_mnmajor_sw128(sQ + kk * 2048, 16384), idG,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          if (elect_one()) mma_commit(&bar[kQEmpty + st]);
+          if (i + 1 < n) issue_dp(i + 1);
+        } else {
+          // dK += dS^T Q with dS^T from shared memory (keys x queries, K-major), then
+          // dQ = dS K into the dP^T columns, which the elementwise warps have read:
+          // A = the same tile read queries-major, B = K read d-major.
+          constexpr uint32_t idQ = idesc_bf16(128, D, true, true);
+          const uint32_t sdS = smem_u32(sm + L::kdS);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            if (elect_one()) mma_ss(tmem + kColdK, desc_kmajor_sw128(sdS + off), desc_mnmajor_sw128(sQ + kk * 2048, 16384),
+                                    idG, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            if (elect_one()) mma_ss(tmem + kColdP, desc_mnmajor_sw128(sdS + kk * 2048, 16384),
+                                    desc_mnmajor_sw128(sK + kk * 2048, 16384), idQ, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_commit(&bar[kQEmpty + st]);
+          if (elect_one()) mma_commit(&bar[kdQFull]);
+          // the next dP^T goes where this dQ is: wait until it has been read out
+          if (i + 1 < n) {
+            if (!mbar_wait(&bar[kdQFree], i & 1, err, 805)) break;
+            tc_fence_after();
+            issue_dp(i + 1);
+          }
+        }
         if (lane == 0) steps.put(1, i + 1);
       }
       if (elect_one()) mma_commit(&bar[kAccDone]);
@@ -407,11 +455,48 @@ __global__ void __launch_bounds__(320, 1)
             const float2 ds = mul2(make_float2(p[cc], p[cc + 1]), t);
             pk[u] = pack_bf16x2(ds.x, ds.y);
           }
-          tmem_st16(tmem + lane_off + kColdP + cb + ci * 16, pk);
+          if (!FQ) {
+            tmem_st16(tmem + lane_off + kColdP + cb + ci * 16, pk);
+          } else {
+            // row `row` (a key) of the query half `half`, 128-byte swizzled: the
+            // 16-byte chunk j of the row lands at chunk j ^ (row % 8).  The
+            // tile's previous contents were last read by the previous dK/dQ
+            // products, which completed before the previous drain.
+            const uint32_t rowb = smem_u32(sm + L::kdS + half * 16384 + row * 128);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              st_shared_v4(rowb + (((ci * 4 + v) ^ (row & 7)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
-        tmem_st_wait();
+        if (!FQ) {
+          tmem_st_wait();
+        } else {
+          fence_proxy_async_smem();  // the tensor cores read the tile through the async proxy
+        }
         tc_fence_before();
         mbar_arrive(&bar[kdSReady]);
+        if (FQ) {
+          // drain this tile's dQ (query rows on the TMEM lanes, d on the columns)
+          // into the fp32 accumulator; the dP^T columns are then free again
+          if (!mbar_wait(&bar[kdQFull], i & 1, err, 905)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t r[D / 2];
+#pragma unroll
+          for (int ci = 0; ci < D / 64; ++ci)
+            tmem_ld32(tmem + lane_off + kColdP + half * (D / 2) + ci * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[ci * 32]));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bar[kdQFree]);
+          const int q = it.q0() + row;
+          const int h = it.head(R);
+          if (q < it.seg_end && check(q >= 0 && q < s.T && h < s.Hq, err, 1108)) {
+            float* base = dq_acc + (static_cast<size_t>(h) * (D / 4) + half * (D / 8)) * s.T * 4 + static_cast<size_t>(q) * 4;
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v)
+              red_add_v4(base + static_cast<size_t>(v) * s.T * 4, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          }
+        }
         if (row == 0) steps.put(2 + half, i + 1);
       }
     }
@@ -494,16 +579,19 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D>
+template <int D, bool FQ>
 cudaError_t launch_dkdv_d(const Sched& s, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                           const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dk, void* dv,
-                          float* acc_k, float* acc_v, int deterministic, unsigned int* err, cudaStream_t stream) {
-  using L = DkdvLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+                          float* acc_k, float* acc_v, float* dq_acc, int deterministic, unsigned int* err,
+                          cudaStream_t stream) {
+  using L = DkdvLayout<D, FQ>;
+  static_assert(L::kBytes <= 232448, "shared memory of one CTA");
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, FQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hkv);
-  dkdv_kernel<D><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
-                                                   static_cast<__nv_bfloat16*>(dv), acc_k, acc_v, deterministic, err);
+  dkdv_kernel<D, FQ><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
+                                                       static_cast<__nv_bfloat16*>(dv), acc_k, acc_v, dq_acc,
+                                                       deterministic, err);
   return cudaGetLastError();
 }
 
@@ -511,11 +599,17 @@ cudaError_t launch_dkdv_d(const Sched& s, const CUtensorMap& mQ, const CUtensorM
 
 cudaError_t launch_dkdv(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                         const CUtensorMap& mdO, const float* lse, const float* Dvec, void* dk, void* dv,
-                        float* acc_k, float* acc_v, int deterministic, unsigned int* err, cudaStream_t stream) {
+                        float* acc_k, float* acc_v, float* dq_acc, int deterministic, unsigned int* err,
+                        cudaStream_t stream) {
   if (s.num_items == 0) return cudaSuccess;
-  return d == 64 ? launch_dkdv_d<64>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, deterministic, err, stream)
-                 : launch_dkdv_d<128>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, deterministic, err,
-                                      stream);
+  if (dq_acc != nullptr)
+    return d == 64 ? launch_dkdv_d<64, true>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, dq_acc, 0, err, stream)
+                   : launch_dkdv_d<128, true>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, dq_acc, 0, err,
+                                              stream);
+  return d == 64 ? launch_dkdv_d<64, false>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, nullptr,
+                                            deterministic, err, stream)
+                 : launch_dkdv_d<128, false>(s, mQ, mK, mV, mdO, lse, Dvec, dk, dv, acc_k, acc_v, nullptr,
+                                             deterministic, err, stream);
 }
 
 }  // namespace dkv

@@ -28,11 +28,20 @@ cudaError_t launch_dq(const Sched& s, int d, const CUtensorMap& mQ, const CUtens
 // dK/dV: one (key tile, kv-head, split) item per CTA.  Response key rows are
 // written to dk/dv (bf16); prompt key rows go to fp32 `acc_k/acc_v`
 // ([P,Hkv,d]) with atomics when `deterministic` is 0, or to the split's slice
-// of `part_k/part_v` ([S,P,Hkv,d]) when it is 1.
+// of `part_k/part_v` ([S,P,Hkv,d]) when it is 1.  With `dq_acc` not null
+// (atomic mode only) the kernel also adds every tile's dQ (unscaled) to the
+// fp32 accumulator dq_acc [Hq][d/4][T][4], which must start at zero.
 cudaError_t launch_dkdv(const Sched& s, int d, const CUtensorMap& mQ, const CUtensorMap& mK,
                         const CUtensorMap& mV, const CUtensorMap& mdO, const float* lse, const float* Dvec,
-                        void* dk, void* dv, float* acc_k, float* acc_v, int deterministic,
+                        void* dk, void* dv, float* acc_k, float* acc_v, float* dq_acc, int deterministic,
                         unsigned int* err, cudaStream_t stream);
+
+// dq [T,Hq,d] bf16 = scale * dq_acc ([Hq][d/4][T][4] fp32), RNE.  Rows t <
+// prompt_end outside [keep_lo, keep_hi) are left untouched; when dq_prompt
+// is not null, rows t < prompt_end inside it are also written there in fp32
+// ([prompt_end, Hq, d]).
+cudaError_t launch_dq_cast(const float* dq_acc, void* dq, float* dq_prompt, int64_t T, int Hq, int d, float scale,
+                           int64_t prompt_end, int64_t keep_lo, int64_t keep_hi, cudaStream_t stream);
 
 // Where each group's prompt rows sit: accumulator rows [acc_row[g],
 // acc_row[g+1]) hold the prompt that starts at packed row packed_row[g].
@@ -50,6 +59,10 @@ struct PromptMap {
 cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsplit, size_t slice,
                                  void* dk, void* dv, float* f32_k, float* f32_v, const PromptMap& map,
                                  int row_elems, unsigned int* err, cudaStream_t stream);
+
+// Device address of the library's error word on the current device (looked
+// up once per device), or null.
+unsigned int* device_error_word();
 
 // Self-test of the bounded waits: a wait on an mbarrier phase that never
 // completes gives up after limit_ns and records a timeout at `site`.

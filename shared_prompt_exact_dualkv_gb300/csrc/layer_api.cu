@@ -1,9 +1,7 @@
 // C ABI of the packed decoder layer (include/dualkv_layer.h): argument
 // checks, the workspace layout, and the launch sequence of the forward and
-// backward passes.  GEMMs go to cuBLAS; everything else runs in this
+// backward passes.  Every step, GEMMs included (gemm.cu), runs in this
 // library's kernels on the caller's stream.
-#include <cublas_v2.h>
-
 #include <algorithm>
 #include <cmath>
 #include <memory>
@@ -11,12 +9,11 @@
 
 #include "../../include/dualkv.h"
 #include "../../include/dualkv_layer.h"
+#include "kernels.h"
 #include "layer_kernels.h"
 
 namespace dkv {
 namespace {
-
-constexpr size_t kCublasScratch = size_t(32) << 20;
 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -83,7 +80,7 @@ struct LayerWs {
   // forward transient, reused by the backward as dqkv
   size_t qkv;
   // backward scratch (dm reuses m; dgu is written over gu)
-  size_t dh2, dx2, da, dq, dk, dv, dh1, part, attn, cublas;
+  size_t dh2, dx2, da, dq, dk, dv, dh1, part, attn;
   size_t attn_bytes, total;
 };
 
@@ -119,7 +116,6 @@ LayerWs layout(const dualkv_layer_config& c, int64_t T, size_t attn_bytes) {
   w.part = take(size_t(rmsnorm_bwd_blocks()) * H * 4);
   w.attn_bytes = attn_bytes;
   w.attn = take(std::max<size_t>(attn_bytes, 256));
-  w.cublas = take(kCublasScratch);
   w.total = o;
   return w;
 }
@@ -129,67 +125,31 @@ size_t attention_ws_bytes(const dualkv_layer_config& c, int32_t G, const int64_t
   return dualkv_bwd_groups_workspace_bytes(G, P, N, R, c.Hq, c.Hkv, c.d, 0, 0);
 }
 
-constexpr int kMaxDevices = 64;
-
-// One cuBLAS handle per host thread and device, created on first use.
-cublasHandle_t handle_for_device() {
-  thread_local cublasHandle_t handles[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!handles[dev]) {
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    handles[dev] = h;
-  }
-  return handles[dev];
-}
-
-// Row-major GEMMs written in cuBLAS's column-major terms.
+// The layer's row-major GEMMs on the library's tensor-core kernels (gemm.cu),
+// all on one stream; the first failure sticks.
 struct Gemm {
-  cublasHandle_t h;
+  cudaStream_t stream = nullptr;
+  unsigned int* err = nullptr;
   bool ok = true;
 
   // Y[rows, out] (+)= X[rows, in] . W[out, in]^T
   void xwT(int64_t rows, int out, int in, const void* X, const void* W, void* Y, float beta) {
-    if (!ok || rows == 0) return;
-    const float alpha = 1.f;
-    ok = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, out, static_cast<int>(rows), in, &alpha, W, CUDA_R_16BF, in, X,
-                      CUDA_R_16BF, in, &beta, Y, CUDA_R_16BF, out, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+    if (ok) ok = gemm_xwT(rows, out, in, X, W, Y, beta != 0.f, err, stream) == cudaSuccess;
   }
   // dX[rows, in] = dY[rows, out] . W[out, in]
   void dyW(int64_t rows, int out, int in, const void* dY, const void* W, void* dX) {
-    if (!ok || rows == 0) return;
-    const float alpha = 1.f, beta = 0.f;
-    ok = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, in, static_cast<int>(rows), out, &alpha, W, CUDA_R_16BF, in, dY,
-                      CUDA_R_16BF, out, &beta, dX, CUDA_R_16BF, in, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+    if (ok) ok = gemm_dyW(rows, in, out, dY, W, dX, err, stream) == cudaSuccess;
   }
   // dW[out, in] (fp32) = dY[rows, out]^T . X[rows, in]
   void dW(int64_t rows, int out, int in, const void* dY, const void* X, float* dWp) {
-    if (!ok) return;
-    const float alpha = 1.f, beta = 0.f;
-    if (rows == 0) {
-      ok = cudaMemsetAsync(dWp, 0, size_t(out) * in * 4, stream()) == cudaSuccess;
-      return;
-    }
-    ok = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, in, out, static_cast<int>(rows), &alpha, X, CUDA_R_16BF, in, dY,
-                      CUDA_R_16BF, out, &beta, dWp, CUDA_R_32F, in, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
-  }
-  cudaStream_t stream() {
-    cudaStream_t s = nullptr;
-    cublasGetStream(h, &s);
-    return s;
+    if (ok) ok = gemm_dW(out, in, rows, dY, X, dWp, err, stream) == cudaSuccess;
   }
 };
 
-int begin_gemms(Gemm* g, cudaStream_t st, uint8_t* ws, const LayerWs& L) {
-  g->h = handle_for_device();
-  if (!g->h) return DUALKV_ERR_CUDA;
-  if (cublasSetStream(g->h, st) != CUBLAS_STATUS_SUCCESS) return DUALKV_ERR_CUDA;
-  if (cublasSetWorkspace(g->h, ws + L.cublas, kCublasScratch) != CUBLAS_STATUS_SUCCESS) return DUALKV_ERR_CUDA;
-  return DUALKV_OK;
+int begin_gemms(Gemm* g, cudaStream_t st) {
+  g->stream = st;
+  g->err = device_error_word();
+  return g->err ? DUALKV_OK : DUALKV_ERR_CUDA;
 }
 
 int weights_ok(const dualkv_layer_weights* w) {
@@ -258,7 +218,7 @@ int dualkv_layer_fwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   std::unique_ptr<RowMap> map(new RowMap);
   fill_rowmap(map.get(), G, P, N, R_lens);
   Gemm gm;
-  if ((st = begin_gemms(&gm, cs, ws, L)) != DUALKV_OK) return st;
+  if ((st = begin_gemms(&gm, cs)) != DUALKV_OK) return st;
 
   cudaError_t e = launch_rmsnorm_fwd(x, w->ln1, ws + L.h1, reinterpret_cast<float*>(ws + L.r1), T, H, c.eps, cs);
   if (e != cudaSuccess) return DUALKV_ERR_CUDA;
@@ -318,7 +278,7 @@ int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   std::unique_ptr<RowMap> map(new RowMap);
   fill_rowmap(map.get(), G, P, N, R_lens);
   Gemm gm;
-  if ((st = begin_gemms(&gm, cs, ws, L)) != DUALKV_OK) return st;
+  if ((st = begin_gemms(&gm, cs)) != DUALKV_OK) return st;
 
   // MLP: dWd, dm (over m), dgu (over gu), dWgu, dh2
   gm.dW(T, H, I, dy, ws + L.m, grads->wd);
@@ -352,6 +312,34 @@ int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   // first norm: dx = dx2 + RMSNorm'(dh1)
   e = launch_rmsnorm_bwd(ws + L.dh1, x, w->ln1, reinterpret_cast<const float*>(ws + L.r1), ws + L.dx2, dx,
                          reinterpret_cast<float*>(ws + L.part), grads->ln1, T, H, cs);
+  return cuda_status(e);
+}
+
+int dualkv_gemm(int32_t kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* Y,
+                int32_t accumulate, void* stream) {
+  if (kind < 0 || kind > 2 || M < 0 || N < 0 || K < 0) return DUALKV_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || N > lim || K > lim) return DUALKV_ERR_INVALID_ARG;
+  // row lengths of A, B and Y
+  const int64_t la = kind == 2 ? M : K, lb = kind == 0 ? K : N;
+  if (la % 8 || lb % 8 || N % 8) return DUALKV_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return DUALKV_OK;
+  if (!Y || (K > 0 && (!A || !B))) return DUALKV_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(Y)) return DUALKV_ERR_ALIGNMENT;
+  unsigned int* err = device_error_word();
+  if (!err) return DUALKV_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (kind == 0) {
+    if (K == 0)
+      return accumulate ? DUALKV_OK : cuda_status(cudaMemsetAsync(Y, 0, size_t(M) * N * 2, cs));
+    e = gemm_xwT(M, static_cast<int>(N), static_cast<int>(K), A, B, Y, accumulate != 0, err, cs);
+  } else if (kind == 1) {
+    if (K == 0) return cuda_status(cudaMemsetAsync(Y, 0, size_t(M) * N * 2, cs));
+    e = gemm_dyW(M, static_cast<int>(N), static_cast<int>(K), A, B, Y, err, cs);
+  } else {
+    e = gemm_dW(static_cast<int>(M), static_cast<int>(N), K, A, B, static_cast<float*>(Y), err, cs);
+  }
   return cuda_status(e);
 }
 

@@ -42,4 +42,17 @@ cudaError_t launch_swiglu_fwd(const void* gu, void* m, int64_t rows, int inter, 
 // dgu = [dgate | dup] from dm and gu (dgu may be gu itself).
 cudaError_t launch_swiglu_bwd(const void* gu, const void* dm, void* dgu, int64_t rows, int inter, cudaStream_t st);
 
+// bf16 GEMMs on the tensor cores (gemm.cu); row-major operands, fp32
+// accumulation.  Every column count and K must be a multiple of 8.
+//   gemm_xwT: Y[M,N] = X[M,K] . W[N,K]^T (+ Y when accumulate), bf16 out.
+//   gemm_dyW: dX[M,N] = dY[M,K] . W[K,N], bf16 out.
+//   gemm_dW:  dW[M,N] = dY[K,M]^T . X[K,N], fp32 out (zero when K == 0).
+// `err` is the device error word (bounded pipeline waits record timeouts).
+cudaError_t gemm_xwT(int64_t M, int N, int K, const void* X, const void* W, void* Y, bool accumulate,
+                     unsigned int* err, cudaStream_t stream);
+cudaError_t gemm_dyW(int64_t M, int N, int K, const void* dY, const void* W, void* dX, unsigned int* err,
+                     cudaStream_t stream);
+cudaError_t gemm_dW(int M, int N, int64_t K, const void* dY, const void* X, float* dW, unsigned int* err,
+                    cudaStream_t stream);
+
 }  // namespace dkv

@@ -91,6 +91,50 @@ __global__ void __launch_bounds__(256) prompt_reduce_kernel(const __grid_constan
   }
 }
 
+// dq = scale * dq_acc, transposed from [Hq][D/4][T][4] to [T][Hq][D]: one
+// block per 32 rows of one head, staged through shared memory so that both
+// the reads (32 consecutive rows of a 4-column chunk) and the writes (whole
+// rows of the head) are contiguous.
+template <int D>
+__global__ void __launch_bounds__(256) dq_cast_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                                      float* __restrict__ dq_prompt, int64_t T, int Hq, float scale,
+                                                      int64_t prompt_end, int64_t keep_lo, int64_t keep_hi) {
+  __shared__ float4 tile[32][D / 4 + 1];
+  const int h = blockIdx.y;
+  const int64_t t0 = int64_t(blockIdx.x) * 32;
+  const int tid = threadIdx.x;
+  for (int c = tid / 32; c < D / 4; c += 8) {
+    const int64_t t = t0 + (tid % 32);
+    tile[tid % 32][c] = t < T ? acc[(int64_t(h) * (D / 4) + c) * T + t] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncthreads();
+  constexpr int kParts = D / 16;  // 16 columns per thread
+  for (int i = tid; i < 32 * kParts; i += 256) {
+    const int r = i / kParts, part = i % kParts;
+    const int64_t t = t0 + r;
+    if (t >= T || (t < prompt_end && (t < keep_lo || t >= keep_hi))) continue;
+    float f[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 v = tile[r][part * 4 + u];
+      f[4 * u] = v.x * scale;
+      f[4 * u + 1] = v.y * scale;
+      f[4 * u + 2] = v.z * scale;
+      f[4 * u + 3] = v.w * scale;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(dq + (t * Hq + h) * D + part * 16);
+    dst[0] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                        pack_bf16x2(f[6], f[7]));
+    dst[1] = make_uint4(pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]), pack_bf16x2(f[12], f[13]),
+                        pack_bf16x2(f[14], f[15]));
+    if (dq_prompt != nullptr && t < prompt_end) {
+      float4* d32 = reinterpret_cast<float4*>(dq_prompt + (t * Hq + h) * D + part * 16);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) d32[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
+    }
+  }
+}
+
 // One thread waits, with the kernels' own bounded wait, for an mbarrier
 // phase that nothing completes; the wait gives up after limit_ns, records a
 // timeout at `site` in the error word and the kernel returns normally.
@@ -129,6 +173,21 @@ cudaError_t launch_preprocess(const void* out, const void* dout, float* Dvec, in
     preprocess_kernel<8><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
                                                    Dvec, rows, static_cast<int>(T), Hq,
                                                    reinterpret_cast<float4*>(zero_ptr), z4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_cast(const float* dq_acc, void* dq, float* dq_prompt, int64_t T, int Hq, int d, float scale,
+                           int64_t prompt_end, int64_t keep_lo, int64_t keep_hi, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>(Hq));
+  if (d == 64)
+    dq_cast_kernel<64><<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                 static_cast<__nv_bfloat16*>(dq), dq_prompt, T, Hq, scale, prompt_end,
+                                                 keep_lo, keep_hi);
+  else
+    dq_cast_kernel<128><<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                  static_cast<__nv_bfloat16*>(dq), dq_prompt, T, Hq, scale,
+                                                  prompt_end, keep_lo, keep_hi);
   return cudaGetLastError();
 }
 

@@ -45,4 +45,21 @@ inline bool make_map_thd(CUtensorMap* m, const void* base, int64_t T, int H, int
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a row-major [rows, cols] bf16 matrix (cols contiguous, a
+// multiple of 8).  One box is box_cols (64: 128 B, one swizzle row) x
+// box_rows, landing as box_rows 128-byte rows with the 128-byte swizzle.
+// Elements past either extent read as zero.
+inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || rows < 1 || cols < 1 || cols % 8 != 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dkv

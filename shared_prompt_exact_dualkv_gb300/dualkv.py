@@ -32,7 +32,7 @@ EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_st
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
             "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
             "dualkv_packed_positions", "dualkv_selftest_wait_timeout", "dualkv_fwd_partial", "dualkv_bwd_partial",
-            "dualkv_checks_enabled")
+            "dualkv_checks_enabled", "dualkv_gemm")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -114,6 +114,8 @@ def _load() -> ctypes.CDLL:
                                        ctypes.c_int, c_i32, c_i64, c_i64, c_p, ctypes.c_size_t, c_p, c_p, c_p, c_p,
                                        c_p, c_p, c_p]
     lib.dualkv_bwd_partial.restype = ctypes.c_int
+    lib.dualkv_gemm.argtypes = [c_i32, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_i32, c_p]
+    lib.dualkv_gemm.restype = ctypes.c_int
     lib.dualkv_checks_enabled.argtypes = []
     lib.dualkv_checks_enabled.restype = ctypes.c_int
     lib.dualkv_version.argtypes = []
@@ -149,6 +151,19 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+BWD_ATOMIC = 0          # fp32 atomics; dQ fused into the dK/dV kernel
+BWD_DETERMINISTIC = 1   # fixed-order sums, separate dQ kernel, bitwise reproducible
+BWD_ATOMIC_SPLIT_DQ = 2  # fp32 atomics for prompt dK/dV, separate dQ kernel
+
+
+def _mode(deterministic) -> int:
+    """The backward mode: False/True map to BWD_ATOMIC/BWD_DETERMINISTIC; an
+    int is passed through."""
+    if isinstance(deterministic, bool):
+        return BWD_DETERMINISTIC if deterministic else BWD_ATOMIC
+    return int(deterministic)
+
+
 def _check(st: int, where: str) -> None:
     if st != DUALKV_OK:
         raise DualKVError(st, where)
@@ -169,7 +184,7 @@ def dualkv_fwd(q, k, v, P: int, R_lens: Sequence[int], out, lse, softmax_scale: 
 def dualkv_bwd_workspace_bytes(P: int, R_lens: Sequence[int], Hq: int, Hkv: int, d: int,
                                deterministic: bool, num_splits: int = 0) -> int:
     return int(lib.dualkv_bwd_workspace_bytes(int(P), len(R_lens), _lens(R_lens), int(Hq), int(Hkv), int(d),
-                                              1 if deterministic else 0, int(num_splits)))
+                                              _mode(deterministic), int(num_splits)))
 
 
 def dualkv_bwd(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_scale: float,
@@ -181,7 +196,7 @@ def dualkv_bwd(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], softmax_s
     Hkv = k.shape[1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.dualkv_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P), len(R_lens),
-                        _lens(R_lens), Hq, Hkv, d, float(softmax_scale), 1 if deterministic else 0,
+                        _lens(R_lens), Hq, Hkv, d, float(softmax_scale), _mode(deterministic),
                         int(num_splits), _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk), _ptr(dv),
                         _stream(stream))
     if check:
@@ -200,7 +215,7 @@ def dualkv_bwd_static_workspace(q, k, v, out, dout, lse, P: int, R_lens: Sequenc
     Hkv = k.shape[1]
     st = lib.dualkv_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P),
                                          len(R_lens), _lens(R_lens), Hq, Hkv, d, float(softmax_scale),
-                                         1 if deterministic else 0, int(num_splits), _ptr(dq), _ptr(dk), _ptr(dv),
+                                         _mode(deterministic), int(num_splits), _ptr(dq), _ptr(dk), _ptr(dv),
                                          _stream(stream))
     if check:
         _check(st, "dualkv_bwd_static_workspace")
@@ -231,7 +246,7 @@ def dualkv_bwd_partial(q, k, v, out, dout, lse, P: int, R_lens: Sequence[int], p
     lo, hi = prompt_rows
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.dualkv_bwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), int(P), len(R_lens),
-                                _lens(R_lens), Hq, Hkv, d, float(softmax_scale), 1 if deterministic else 0,
+                                _lens(R_lens), Hq, Hkv, d, float(softmax_scale), _mode(deterministic),
                                 int(num_splits), int(lo), int(hi), _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk),
                                 _ptr(dv), _ptr(dq_prompt), _ptr(dk_prompt), _ptr(dv_prompt), _stream(stream))
     if check:
@@ -265,7 +280,7 @@ def dualkv_bwd_groups_workspace_bytes(groups, Hq: int, Hkv: int, d: int, determi
                                       num_splits: int = 0) -> int:
     G, Ps, Ns, Rs = _groups(groups)
     return int(lib.dualkv_bwd_groups_workspace_bytes(G, Ps, Ns, Rs, int(Hq), int(Hkv), int(d),
-                                                     1 if deterministic else 0, int(num_splits)))
+                                                     _mode(deterministic), int(num_splits)))
 
 
 def dualkv_bwd_groups(q, k, v, out, dout, lse, groups, softmax_scale: float, deterministic: bool, workspace,
@@ -276,10 +291,29 @@ def dualkv_bwd_groups(q, k, v, out, dout, lse, groups, softmax_scale: float, det
     G, Ps, Ns, Rs = _groups(groups)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.dualkv_bwd_groups(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), G, Ps, Ns, Rs, Hq,
-                               Hkv, d, float(softmax_scale), 1 if deterministic else 0, int(num_splits),
+                               Hkv, d, float(softmax_scale), _mode(deterministic), int(num_splits),
                                _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
     if check:
         _check(st, "dualkv_bwd_groups")
+    return st
+
+
+def dualkv_gemm(kind: int, A, B, Y, accumulate: bool = False, stream=None, check: bool = True) -> int:
+    """The layer's tensor-core GEMM: kind 0 Y = A.B^T (+ Y), kind 1 Y = A.B,
+    kind 2 Y (fp32) = A^T.B; A, B bf16 row-major device tensors."""
+    if kind == 0:
+        M, K = A.shape
+        N = B.shape[0]
+    elif kind == 1:
+        M, K = A.shape
+        N = B.shape[1]
+    else:
+        K, M = A.shape
+        N = B.shape[1]
+    st = lib.dualkv_gemm(int(kind), int(M), int(N), int(K), _ptr(A), _ptr(B), _ptr(Y), 1 if accumulate else 0,
+                         _stream(stream))
+    if check:
+        _check(st, "dualkv_gemm")
     return st
 
 

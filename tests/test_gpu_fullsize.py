@@ -130,7 +130,8 @@ def test_fullsize_parity(name):
         sdk = dk.float().sum(0).double().cpu().numpy()
         scale_dk = dk.float().abs().sum(0).double().cpu().numpy()
         assert np.all(np.abs(sdk) <= 1e-2 * scale_dk + 1e-3), (det, "sum dK")
-    # both modes agree closely (they differ only in the order of fp32 sums)
+    # both modes agree closely (they differ only in the order of fp32 sums,
+    # then one bf16 rounding)
     for x_, y_ in zip(grads[False], grads[True]):
         diff = float(torch.linalg.vector_norm(x_.float() - y_.float()) / torch.linalg.vector_norm(y_.float()))
-        assert diff <= 1e-3, diff
+        assert diff <= 3e-3, diff

@@ -196,10 +196,11 @@ def _gpu_case():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("det", [False, True], ids=["atomic", "deterministic"])
+@pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic_fused_dq", "deterministic", "atomic_split_dq"])
 def test_partial_entry_points_whole_prompt_equal_regular_calls(det):
     """(lo, hi) = (0, P): bf16 outputs are those of dualkv_fwd/dualkv_bwd bit
-    for bit, and the fp32 prompt rows round (RNE) to the bf16 prompt rows."""
+    for bit (to fp32 summation order where dQ is summed with atomics), and the
+    fp32 prompt rows round (RNE) to the bf16 prompt rows."""
     from shared_prompt_exact_dualkv_gb300 import dualkv as D
     w, x = _gpu_case()
     q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.dout))
@@ -215,7 +216,10 @@ def test_partial_entry_points_whole_prompt_equal_regular_calls(det):
     assert D.dualkv_last_device_error()[0] == 0
     assert torch.equal(out, ro) and torch.equal(lse, rl)
     for a, b in ((dq, rdq), (dk, rdk), (dv, rdv)):
-        assert torch.equal(a, b)
+        if det == 0:   # atomic sums: the order varies from run to run
+            assert ((a.float() - b.float()).norm() / b.float().norm()).item() <= 3e-3
+        else:
+            assert torch.equal(a, b)
     for a, b in zip(f32, (dq, dk, dv)):
         assert torch.equal(a.to(torch.bfloat16), b[:w.P])
 
@@ -280,7 +284,8 @@ def _gpu_rank(rank, world, port, q, divide):
     R_local = list(w.R_lens[lo:hi])
     rows = sharded.prompt_bounds(w.P, world, rank) if divide else None
     out, lse = sharded.sharded_forward(t[0], t[1], t[2], w.P, R_local, w.scale, prompt_rows=rows)
-    dq, dk, dv = sharded.sharded_backward(t[0], t[1], t[2], out, t[3], lse, w.P, R_local, w.scale, prompt_rows=rows)
+    dq, dk, dv = sharded.sharded_backward(t[0], t[1], t[2], out, t[3], lse, w.P, R_local, w.scale, prompt_rows=rows,
+                                          deterministic=True)
     torch.cuda.synchronize()
     q.put((rank, idx.numpy(), out.float().cpu().numpy(), lse.cpu().numpy(), dq.float().cpu().numpy(),
            dk.float().cpu().numpy(), dv.float().cpu().numpy()))
@@ -303,7 +308,7 @@ def test_two_gpu_processes_match_oracle_and_unsharded_run(divide):
     # the forward, and the backward's response rows, are the unsharded run's, bit for bit
     q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, full_do))
     uo, ul = D.forward(q, k, v, w.P, w.R_lens, w.scale)
-    udq, udk, udv = D.backward(q, k, v, uo, do, ul, w.P, w.R_lens, w.scale)
+    udq, udk, udv = D.backward(q, k, v, uo, do, ul, w.P, w.R_lens, w.scale, deterministic=True)
     np.testing.assert_array_equal(out, uo.float().cpu().numpy())
     np.testing.assert_array_equal(lse, ul.cpu().numpy())
     for a, b in ((dq, udq), (dk, udk), (dv, udv)):
