@@ -575,7 +575,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="p32k", choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--deterministic", action="store_true", help="time the deterministic dK/dV mode")
+    ap.add_argument("--deterministic", action="store_true", help="time the deterministic backward (mode 1)")
+    ap.add_argument("--mode", type=int, choices=[0, 1, 2], default=None,
+                    help="backward mode: 0 atomic with dQ fused into dK/dV (default), 1 deterministic, "
+                         "2 atomic prompt dK/dV with a separate dQ kernel")
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
     ap.add_argument("--layer", action="store_true",
                     help="also time a Qwen3-8B-shaped decoder layer, packed against replicated")
@@ -600,7 +603,9 @@ def main():
     out = torch.empty_like(q)
     lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    det = bool(args.deterministic)
+    mode = args.mode if args.mode is not None else (1 if args.deterministic else 0)
+    det = mode   # the backward mode, passed through to dualkv_bwd
+    fused = mode == 0
     ws = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, det), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.current_stream()
@@ -655,16 +660,18 @@ def main():
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
-    # dominant kernel: dK/dV (four products per unmasked pair: S^T, dP^T, dV, dK);
-    # per step, which is per launch whenever the work list fits one launch
+    # dominant kernel: dK/dV (products per unmasked pair: S^T, dP^T, dV, dK, and
+    # dQ in the fused mode); per step, which is per launch whenever the work
+    # list fits one launch
+    dkdv_per_pair = 10 if fused else 8
     dkdv_ms = per_kernel.get("bwd_dkdv", 0.0)
-    dkdv_flops = 8.0 * w.d * w.Hq * w.pairs_per_head()
+    dkdv_flops = float(dkdv_per_pair) * w.d * w.Hq * w.pairs_per_head()
     dkdv_tf = dkdv_flops / (dkdv_ms * 1e-3) / 1e12 if dkdv_ms else None
-    roofline = {"bound": "tensor", "kernel": "dkdv_kernel", "achieved": dkdv_tf, "peak": peak_sus,
-                "unit": "TFLOP/s", "frac": (dkdv_tf / peak_sus) if dkdv_tf else None,
+    roofline = {"bound": "tensor", "kernel": "dkdv_kernel" + ("<fused dQ>" if fused else ""), "achieved": dkdv_tf,
+                "peak": peak_sus, "unit": "TFLOP/s", "frac": (dkdv_tf / peak_sus) if dkdv_tf else None,
                 "traffic": recorded_traffic("dkdv_kernel", w.name, det),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
-                "algorithmic": "8*d flops per unmasked (query,key) pair per q-head",
+                "algorithmic": f"{dkdv_per_pair}*d flops per unmasked (query,key) pair per q-head",
                 "launches_per_step": kernel_launches.get("bwd_dkdv", 0)}
     # The measured sustained rate was taken at the clock its own run settled
     # at; compare per MHz of sampled SM clock as well.
@@ -676,10 +683,10 @@ def main():
                                "frac": (dkdv_tf / run_mhz) / (peak_sus / peak_mhz)}
 
     # every tensor-core kernel against the measured sustained bf16 rate; executed
-    # flops per unmasked pair per q-head: forward 4d, dK/dV 8d, dQ 6d (S and dP
-    # recomputed)
+    # flops per unmasked pair per q-head: forward 4d, dK/dV 8d (10d with dQ
+    # fused), separate dQ 6d (S and dP recomputed)
     tensor_kernels = {}
-    for name, per_pair in (("fwd", 4), ("bwd_dkdv", 8), ("bwd_dq", 6)):
+    for name, per_pair in (("fwd", 4), ("bwd_dkdv", dkdv_per_pair)) + ((() if fused else (("bwd_dq", 6),))):
         kms = per_kernel.get(name, 0.0)
         fl = per_pair * w.d * w.Hq * w.pairs_per_head()
         tf = fl / (kms * 1e-3) / 1e12 if kms else None
@@ -690,15 +697,19 @@ def main():
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     prompt_rows_bytes = w.P * w.Hkv * w.d * 4                      # one fp32 [P, Hkv, d] slice
     n_slices = 1
-    if det and prompt_rows_bytes:
+    if det == 1 and prompt_rows_bytes:
         acc_region = (ws.numel() - align256(w.T * w.Hq * 4)) // 2   # bytes of acc_k (= acc_v)
         n_slices = max(1, acc_region // prompt_rows_bytes)
     hbm_bytes = {
         # read O and dO, write D; zero the two fp32 accumulators in the atomic mode
-        "bwd_preprocess": 2 * w.T * w.Hq * w.d * 2 + w.T * w.Hq * 4 + (0 if det else 2 * prompt_rows_bytes),
+        "bwd_preprocess": (2 * w.T * w.Hq * w.d * 2 + w.T * w.Hq * 4 + (0 if det == 1 else 2 * prompt_rows_bytes)
+                           + (w.T * w.Hq * w.d * 4 if fused else 0)),
         # read every split slice of both accumulators, write bf16 prompt dK and dV
         "bwd_prompt_reduce": 2 * n_slices * prompt_rows_bytes + 2 * w.P * w.Hkv * w.d * 2,
     }
+    if fused:
+        # the dQ cast: read the fp32 accumulator, write bf16 dQ (trace slot of the dQ kernel)
+        hbm_bytes["bwd_dq"] = w.T * w.Hq * w.d * (4 + 2)
     hbm_kernels = {}
     for name, nbytes in hbm_bytes.items():
         kms = per_kernel.get(name, 0.0)
@@ -715,7 +726,7 @@ def main():
                    "R": list(w.R_lens[:1]) if len(set(w.R_lens)) == 1 else list(w.R_lens),
                    "T_packed": w.T, "T_replicated": w.T_replicated, "rho_tokens": round(w.rho_tokens(), 3),
                    "rho_pairs": round(w.rho_pairs(), 3), "useful_tflop_per_step": flops / 1e12,
-                   "dkdv_mode": "deterministic" if det else "atomic",
+                   "dkdv_mode": {0: "atomic, dQ fused", 1: "deterministic", 2: "atomic, separate dQ"}[mode],
                    "l2": "inputs larger than L2 (q alone %.0f MB > 129 MB)" % (q.numel() * 2 / 1e6),
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / peak_sus,
@@ -730,19 +741,23 @@ def main():
     }
 
     if rank == 0 and not args.quick:
-        # the other reduction mode of the prompt dK/dV
-        ws2 = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, not det), dtype=torch.uint8,
-                          device=dev)
-        for _ in range(2):
-            D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, not det, ws2, dq, dk, dv, stream=stream)
+        # the other backward modes on the same inputs (backward alone)
+        names = {0: "atomic_fused_dq", 1: "deterministic", 2: "atomic_split_dq"}
+        others = {}
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(3):
-            D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, not det, ws2, dq, dk, dv, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        result["bwd_ms_other_mode"] = {"mode": "atomic" if det else "deterministic", "ms": a.elapsed_time(b) / 3}
-        del ws2
+        for m in (0, 1, 2):
+            ws2 = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, m), dtype=torch.uint8,
+                              device=dev)
+            for _ in range(2):
+                D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, m, ws2, dq, dk, dv, stream=stream)
+            a.record(stream)
+            for _ in range(3):
+                D.dualkv_bwd(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, m, ws2, dq, dk, dv, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            others[names[m]] = {"bwd_ms": a.elapsed_time(b) / 3, "workspace_bytes": ws2.numel()}
+            del ws2
+        result["bwd_modes"] = others
         # the same library on the replicated N(P+R) layout
         wr = w.replicated()
         gen = torch.Generator(device=dev).manual_seed(7)

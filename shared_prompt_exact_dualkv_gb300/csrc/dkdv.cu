@@ -116,29 +116,41 @@ struct QRuns {
   }
 };
 
+// Walk order of one key-tile item, per q-head of the group: the query tiles
+// of the responses in its chunk first, ascending, then (split 0 of a prompt
+// key tile) the prompt's own query tiles, descending from the last to the
+// key tile's diagonal.  Every prompt key tile of a group walks the responses
+// in the same order, so the CTAs that run together work on the same query
+// tiles at about the same time and L2 serves those tiles (and, with dQ fused,
+// takes their dQ reductions) for all of them.
 struct QIter {
-  int32_t hh, r, t;
-  int32_t q_first, t_end, seg_end;
+  int32_t hh, r, t, step, t_stop;   // t runs from its first tile by `step` until it reaches t_stop
+  int32_t q_first, seg_end;
   int32_t diag_t;   // the query tile on the key tile's diagonal (-1: none in this run)
 
+  __device__ __forceinline__ int32_t resp_runs(const QRuns& R) const { return R.num_runs - R.has_prompt; }
+
   __device__ __forceinline__ void load_run(const Sched& s, const QRuns& R) {
-    if (R.has_prompt && r == 0) {
-      q_first = s.off[R.seg];
-      t = max(R.j, s.pq_lo);
-      t_end = min(R.nP, s.pq_hi);
-      seg_end = s.off[R.seg + 1];
-      diag_t = R.j;
-    } else {
-      const int i = R.seq_lo + r - R.has_prompt;
+    if (r < resp_runs(R)) {
+      const int i = R.seq_lo + r;
       q_first = s.off[i];
       t = R.prompt_item ? 0 : R.j;
-      t_end = s.seg_tiles(i);
+      t_stop = s.seg_tiles(i);
+      step = 1;
       seg_end = s.off[i + 1];
       diag_t = R.prompt_item ? -1 : R.j;
+    } else {
+      q_first = s.off[R.seg];
+      t = min(R.nP, s.pq_hi) - 1;
+      t_stop = max(R.j, s.pq_lo) - 1;
+      step = -1;
+      seg_end = s.off[R.seg + 1];
+      diag_t = R.j;
     }
   }
+  __device__ __forceinline__ bool run_done() const { return step > 0 ? t >= t_stop : t <= t_stop; }
   __device__ __forceinline__ void skip_empty(const Sched& s, const QRuns& R) {
-    while (t >= t_end) {
+    while (run_done()) {
       if (++r == R.num_runs) {
         r = 0;
         ++hh;
@@ -154,7 +166,7 @@ struct QIter {
     skip_empty(s, R);
   }
   __device__ __forceinline__ void next(const Sched& s, const QRuns& R) {
-    ++t;
+    t += step;
     skip_empty(s, R);
   }
   __device__ __forceinline__ int32_t q0() const { return q_first + t * kTile; }
