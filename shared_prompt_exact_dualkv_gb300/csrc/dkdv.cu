@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(320, 1)
     const int cb = half * 64;  // first query column of this thread
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = s.scale_log2;
+    const bool key_in = R.k0 + row < R.k_end;
     bool ok = n > 0;
     if (ok) {
       QIter it;
@@ -439,6 +440,12 @@ __global__ void __launch_bounds__(320, 1)
         if (it.diag()) {
 #pragma unroll
           for (int u = 0; u < 64; ++u) p[u] = (cb + u < row) ? 0.f : p[u];
+        }
+        if (FQ && !key_in) {
+          // a key lane past the item's segment (the ragged end of a prompt
+          // tile holds the first keys of the next segment) must not reach dQ
+#pragma unroll
+          for (int u = 0; u < 64; ++u) p[u] = 0.f;
         }
         {
           uint32_t pk[32];
