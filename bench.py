@@ -577,8 +577,8 @@ def main():
     ap.add_argument("--workload", default="p32k", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--deterministic", action="store_true", help="time the deterministic backward (mode 1)")
     ap.add_argument("--mode", type=int, choices=[0, 1, 2], default=None,
-                    help="backward mode: 0 atomic with dQ fused into dK/dV (default), 1 deterministic, "
-                         "2 atomic prompt dK/dV with a separate dQ kernel")
+                    help="backward mode: 0 atomic prompt dK/dV with a separate dQ kernel (default), "
+                         "1 deterministic, 2 atomic with dQ fused into dK/dV")
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
     ap.add_argument("--layer", action="store_true",
                     help="also time a Qwen3-8B-shaped decoder layer, packed against replicated")
@@ -605,7 +605,7 @@ def main():
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     mode = args.mode if args.mode is not None else (1 if args.deterministic else 0)
     det = mode   # the backward mode, passed through to dualkv_bwd
-    fused = mode == 0
+    fused = mode == 2
     ws = torch.empty(D.dualkv_bwd_workspace_bytes(w.P, w.R_lens, w.Hq, w.Hkv, w.d, det), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.current_stream()
@@ -726,7 +726,7 @@ def main():
                    "R": list(w.R_lens[:1]) if len(set(w.R_lens)) == 1 else list(w.R_lens),
                    "T_packed": w.T, "T_replicated": w.T_replicated, "rho_tokens": round(w.rho_tokens(), 3),
                    "rho_pairs": round(w.rho_pairs(), 3), "useful_tflop_per_step": flops / 1e12,
-                   "dkdv_mode": {0: "atomic, dQ fused", 1: "deterministic", 2: "atomic, separate dQ"}[mode],
+                   "dkdv_mode": {0: "atomic, separate dQ", 1: "deterministic", 2: "atomic, dQ fused"}[mode],
                    "l2": "inputs larger than L2 (q alone %.0f MB > 129 MB)" % (q.numel() * 2 / 1e6),
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / peak_sus,
@@ -742,7 +742,7 @@ def main():
 
     if rank == 0 and not args.quick:
         # the other backward modes on the same inputs (backward alone)
-        names = {0: "atomic_fused_dq", 1: "deterministic", 2: "atomic_split_dq"}
+        names = {0: "atomic", 1: "deterministic", 2: "atomic_fused_dq"}
         others = {}
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for m in (0, 1, 2):

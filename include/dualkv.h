@@ -90,19 +90,20 @@ DUALKV_API int dualkv_fwd(const void* q, const void* k, const void* v, int64_t P
 /*
  * Backward modes: the `deterministic` argument of the backward calls.
  *   DUALKV_BWD_ATOMIC (0): the prompt's dK/dV are summed over the sequences
- *     with fp32 atomics (research-map page, "Approach"), and dQ is computed in
- *     the same kernel as dK/dV, each key tile adding its share of dQ with fp32
- *     atomics; the workspace then also holds an fp32 dQ accumulator of
- *     T*Hq*d*4 bytes.  Results vary in the last bits from run to run.
+ *     with fp32 atomics (research-map page, "Approach"); dQ comes from a
+ *     separate kernel with one writer per row.
  *   DUALKV_BWD_DETERMINISTIC (1): per-split fp32 partials summed in a fixed
- *     order, and dQ from a separate kernel with one writer per row; bitwise
- *     reproducible.
- *   DUALKV_BWD_ATOMIC_SPLIT_DQ (2): prompt dK/dV with fp32 atomics, dQ from
- *     the separate kernel (the smallest workspace).
+ *     order; bitwise reproducible.
+ *   DUALKV_BWD_ATOMIC_FUSED_DQ (2): as mode 0, but dQ is computed in the
+ *     dK/dV kernel, each key tile adding its share of dQ with fp32 atomics
+ *     (no recomputation of S and dP); the workspace then also holds an fp32
+ *     dQ accumulator of T*Hq*d*4 bytes, and dQ varies in the last bits from
+ *     run to run.  On GB300 it is slower than mode 0 (the reductions stall
+ *     the kernel); it is kept for comparison.
  */
 #define DUALKV_BWD_ATOMIC 0
 #define DUALKV_BWD_DETERMINISTIC 1
-#define DUALKV_BWD_ATOMIC_SPLIT_DQ 2
+#define DUALKV_BWD_ATOMIC_FUSED_DQ 2
 
 /*
  * Workspace bytes that dualkv_bwd needs for this shape and backward mode
@@ -122,7 +123,7 @@ DUALKV_API size_t dualkv_bwd_workspace_bytes(int64_t P, int32_t N, const int32_t
  *                       carry the summed gradient of the shared rows).
  *   deterministic     : the backward mode, DUALKV_BWD_ATOMIC (0),
  *                       DUALKV_BWD_DETERMINISTIC (1, bitwise reproducible) or
- *                       DUALKV_BWD_ATOMIC_SPLIT_DQ (2); other values are
+ *                       DUALKV_BWD_ATOMIC_FUSED_DQ (2); other values are
  *                       DUALKV_ERR_INVALID_ARG.
  *   num_splits        : sequence chunks per prompt key tile (0 = library
  *                       choice; must match the value given to

@@ -242,11 +242,11 @@ int resolve_splits(const Shape& sh, int32_t num_splits) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Backward modes (the `deterministic` argument of the ABI).
-constexpr int kModeAtomic = DUALKV_BWD_ATOMIC;              // fp32 atomics, dQ fused into the dK/dV kernel
+constexpr int kModeAtomic = DUALKV_BWD_ATOMIC;                // fp32 atomics for prompt dK/dV, separate dQ kernel
 constexpr int kModeDeterministic = DUALKV_BWD_DETERMINISTIC;
-constexpr int kModeSplitDq = DUALKV_BWD_ATOMIC_SPLIT_DQ;    // fp32 atomics for prompt dK/dV, separate dQ kernel
+constexpr int kModeFusedDq = DUALKV_BWD_ATOMIC_FUSED_DQ;      // fp32 atomics, dQ fused into the dK/dV kernel
 
-bool mode_ok(int mode) { return mode == kModeAtomic || mode == kModeDeterministic || mode == kModeSplitDq; }
+bool mode_ok(int mode) { return mode == kModeAtomic || mode == kModeDeterministic || mode == kModeFusedDq; }
 
 struct WsLayout {
   size_t D = 0, acc_k = 0, acc_v = 0, dq_acc = 0, total = 0;
@@ -267,7 +267,7 @@ WsLayout workspace_layout(const Shape& sh, int mode, int S) {
   w.acc_k = align256(size_t(sh.T) * sh.Hq * 4);
   w.acc_v = w.acc_k + align256(w.acc_floats * 4);
   w.dq_acc = w.acc_v + align256(w.acc_floats * 4);
-  w.total = w.dq_acc + (mode == kModeAtomic ? align256(size_t(sh.T) * sh.Hq * sh.d * 4) : 0);
+  w.total = w.dq_acc + (mode == kModeFusedDq ? align256(size_t(sh.T) * sh.Hq * sh.d * 4) : 0);
   return w;
 }
 
@@ -419,7 +419,7 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   const int mode = deterministic;
   if (!mode_ok(mode)) return DUALKV_ERR_INVALID_ARG;
   const int det = mode == kModeDeterministic ? 1 : 0;
-  const bool fused = mode == kModeAtomic;
+  const bool fused = mode == kModeFusedDq;
   const int S = resolve_splits(sh, num_splits);
   const WsLayout ws = workspace_layout(sh, mode, S);
   if (!workspace || workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;

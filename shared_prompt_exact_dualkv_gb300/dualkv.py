@@ -151,9 +151,9 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-BWD_ATOMIC = 0          # fp32 atomics; dQ fused into the dK/dV kernel
-BWD_DETERMINISTIC = 1   # fixed-order sums, separate dQ kernel, bitwise reproducible
-BWD_ATOMIC_SPLIT_DQ = 2  # fp32 atomics for prompt dK/dV, separate dQ kernel
+BWD_ATOMIC = 0           # fp32 atomics for prompt dK/dV, separate dQ kernel
+BWD_DETERMINISTIC = 1    # fixed-order sums, bitwise reproducible
+BWD_ATOMIC_FUSED_DQ = 2  # fp32 atomics, dQ fused into the dK/dV kernel (slower on GB300)
 
 
 def _mode(deterministic) -> int:

@@ -110,10 +110,10 @@ def test_workspace_bytes(D, P, R, Hq, Hkv, d):
     T = P + sum(R)
     slice_ = P * Hkv * d * 4
     atomic = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, False, 0)
-    # the fused mode adds the fp32 dQ accumulator [Hq][d/4][T][4]
-    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_) + _align256(T * Hq * d * 4)
-    split_dq = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, 2, 0)
-    assert split_dq == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    # the fused-dQ mode adds the fp32 dQ accumulator [Hq][d/4][T][4]
+    fused = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, 2, 0)
+    assert fused == _align256(T * Hq * 4) + 2 * _align256(slice_) + _align256(T * Hq * d * 4)
     assert D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, 3, 0) == 0
     for S in (1, 2, 3):
         det = D.dualkv_bwd_workspace_bytes(P, R, Hq, Hkv, d, True, S)
@@ -170,8 +170,9 @@ def test_groups_workspace_bytes(D, groups, Hq, Hkv, d):
     T = sum(p + sum(r) for p, r in groups)
     slice_ = sum(p for p, _ in groups) * Hkv * d * 4
     atomic = D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, False, 0)
-    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_) + _align256(T * Hq * d * 4)
-    assert D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, 2, 0) == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    assert atomic == _align256(T * Hq * 4) + 2 * _align256(slice_)
+    assert (D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, 2, 0) ==
+            _align256(T * Hq * 4) + 2 * _align256(slice_) + _align256(T * Hq * d * 4))
     maxN = max(len(r) for _, r in groups)
     for S in (1, 2, 3):
         det = D.dualkv_bwd_groups_workspace_bytes(groups, Hq, Hkv, d, True, S)

@@ -66,7 +66,7 @@ def test_forward_parity(case, oracle_results):
     check_forward(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, w.name)
 
 
-@pytest.mark.parametrize("deterministic", [0, 1, 2], ids=["atomic_fused_dq", "deterministic", "atomic_split_dq"])
+@pytest.mark.parametrize("deterministic", [0, 1, 2], ids=["atomic", "deterministic", "atomic_fused_dq"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_backward_parity(case, deterministic, oracle_results):
     dk_ = _lib()
@@ -121,16 +121,16 @@ def _rel(x, y):
 
 def test_reduction_modes_agree():
     """The modes differ only in how partial sums are added.  Atomic prompt
-    dK/dV with the separate dQ kernel (mode 2) against the deterministic mode
+    dK/dV with the separate dQ kernel (mode 0) against the deterministic mode
     (1): dQ and the response rows of dK/dV are the same bits, the prompt rows
-    agree to fp32 summation order.  The fused mode (0) sums dQ over key tiles
+    agree to fp32 summation order.  The fused mode (2) sums dQ over key tiles
     with fp32 atomics as well: it agrees with the others to one bf16 rounding
     of a differently ordered fp32 sum."""
     dk_ = _lib()
     w = synthetic.make_workload("modes", 4, 2, 128, 300, (200, 0, 131, 128))
     _, (q, k, v, do) = _device_inputs(w, seed=8)
     out, lse = dk_.forward(q, k, v, w.P, w.R_lens, w.scale)
-    fused, det, split = (dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=m, num_splits=3)
+    split, det, fused = (dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=m, num_splits=3)
                          for m in (0, 1, 2))
     assert dk_.dualkv_last_device_error()[0] == 0
     assert torch.equal(split[0], det[0])

@@ -196,7 +196,7 @@ def _gpu_case():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic_fused_dq", "deterministic", "atomic_split_dq"])
+@pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic", "deterministic", "atomic_fused_dq"])
 def test_partial_entry_points_whole_prompt_equal_regular_calls(det):
     """(lo, hi) = (0, P): bf16 outputs are those of dualkv_fwd/dualkv_bwd bit
     for bit (to fp32 summation order where dQ is summed with atomics), and the
@@ -216,7 +216,7 @@ def test_partial_entry_points_whole_prompt_equal_regular_calls(det):
     assert D.dualkv_last_device_error()[0] == 0
     assert torch.equal(out, ro) and torch.equal(lse, rl)
     for a, b in ((dq, rdq), (dk, rdk), (dv, rdv)):
-        if det == 0:   # atomic sums: the order varies from run to run
+        if det == 2:   # dQ summed with atomics: the order varies from run to run
             assert ((a.float() - b.float()).norm() / b.float().norm()).item() <= 3e-3
         else:
             assert torch.equal(a, b)
@@ -313,10 +313,15 @@ def test_two_gpu_processes_match_oracle_and_unsharded_run(divide):
     np.testing.assert_array_equal(lse, ul.cpu().numpy())
     for a, b in ((dq, udq), (dk, udk), (dv, udv)):
         np.testing.assert_array_equal(a[w.P:], b.float().cpu().numpy()[w.P:])
-    # prompt rows: one rounding of an fp32 sum, against the unsharded run's own
+    # prompt rows against the unsharded run's own.  With the prompt divided,
+    # both runs see the same bf16 dO (the shares' fp32 sum rounded once) and
+    # differ by the fp32 summation order; with the prompt on every rank, each
+    # rank runs on its own bf16 share and the unsharded run on the rounded sum,
+    # a dO difference of up to one bf16 rounding (about 2^-9 relative).
+    bound = 3e-3 if divide else 1e-2
     for a, b in ((dq, udq), (dk, udk), (dv, udv)):
         bb = b.float().cpu().numpy()[:w.P]
-        assert np.linalg.norm(a[:w.P] - bb) <= 2e-3 * np.linalg.norm(bb)
+        assert np.linalg.norm(a[:w.P] - bb) <= bound * np.linalg.norm(bb)
 
 
 def _gpu_head_rank(rank, world, port, q):
