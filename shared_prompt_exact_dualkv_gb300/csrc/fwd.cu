@@ -113,16 +113,12 @@ __device__ __forceinline__ float2 row_exp(uint32_t tS, int lim, float c, float m
   float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   float rr_lo = 0.f, rr_hi = 0.f;
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_sub, -m_sub);
-  // both halves' loads are issued before either is used: one wait covers them
-  uint32_t rr[128];
-  tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-  tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-  tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[64]));
-  tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&rr[96]));
-  tmem_ld_wait();
 #pragma unroll
   for (int hc = 0; hc < 2; ++hc) {
-    const uint32_t* r = rr + hc * 64;
+    uint32_t r[64];
+    tmem_ld32(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld32(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    tmem_ld_wait();
     uint32_t p[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -144,7 +140,7 @@ __device__ __forceinline__ float2 row_exp(uint32_t tS, int lim, float c, float m
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                __nv_bfloat16* __restrict__ out, float* __restrict__ lse, unsigned int* err) {
