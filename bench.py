@@ -582,6 +582,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the other-mode, replicated and CPU oracle legs")
     ap.add_argument("--layer", action="store_true",
                     help="also time a Qwen3-8B-shaped decoder layer, packed against replicated")
+    ap.add_argument("--gemm", action="store_true",
+                    help="also time the layer's GEMM (one shape per operand layout) against cuBLAS on the "
+                         "workload's packed rows")
     ap.add_argument("--groups", action="store_true",
                     help="also time four prompt groups in one call against four single-group calls")
     ap.add_argument("--kernels-only", action="store_true",
@@ -814,6 +817,9 @@ def main():
 
     if rank == 0 and args.groups:
         result["groups"] = groups_leg(D, dev, stream)
+
+    if rank == 0 and args.gemm and not args.layer:
+        result["gemm"] = gemm_leg(D, dev, stream, w.T)
 
     if rank == 0 and args.layer:
         del q, k, v, do, out, lse, dq, dk, dv, ws

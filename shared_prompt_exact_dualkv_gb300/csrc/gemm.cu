@@ -10,11 +10,14 @@
 // (kind 2) results.  With `accumulate` the bf16 result is added to what Y
 // holds (the residual add of the layer).
 //
-// Persistent kernel, one CTA per SM, 128 x 256 output tiles walked with a
+// Persistent kernel, one CTA per SM, output tiles of BM x 256 walked with a
 // stride of the grid.  Warp 0 copies A/B k-blocks (64 deep) with TMA into a
-// 4-stage ring; warp 1 owns TMEM and issues tcgen05.mma (M=128, N=256, K=16)
-// into one of two 256-column accumulators; warps 2-5 drain the other
-// accumulator (TMEM -> registers -> global) while the next tile is computed.
+// ring of stages; warp 1 owns TMEM and issues tcgen05.mma (M=128, N=256,
+// K=16).  With BM = 128 the products go into one of two 256-column
+// accumulators and warps 2-5 drain the other (TMEM -> registers -> global)
+// while the next tile is computed; with BM = 256 two products per k-step
+// (the two 128-row halves of A against one B block) fill both accumulators
+// and warps 2-9 drain them together.
 // Every wait is bounded (an expired wait records a timeout and the kernel
 // returns).
 #include <cuda_bf16.h>
@@ -27,16 +30,27 @@
 namespace dkv {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers, TMEM slot, alignment slack
-constexpr int kEpiThreads = 128;
+constexpr int kBN = 256, kBK = 64;
 
-enum GemmBar { kFull = 0, kEmpty = 4, kAccFull = 8, kAccEmpty = 10, kNumGemmBars = 12 };
+// Tile shapes: BM = 128 rows keeps two 256-column accumulators in TMEM, so
+// the epilogue of one tile overlaps the next tile's products; BM = 256 rows
+// uses both accumulators for one tile (two M = 128 products share every B
+// k-block), which halves the B bytes each SM copies per product flop.
+template <int BM>
+struct GemmCfg {
+  static constexpr int kStages = BM == 128 ? 4 : 3;
+  static constexpr int kBufs = BM == 128 ? 2 : 1;   // accumulators per tile in flight
+  static constexpr int kEpiWarps = BM == 128 ? 4 : 8;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kABytes = BM * kBK * 2;
+  static constexpr int kBBytes = kBN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers, TMEM slot, alignment slack
+};
+
+// barriers: full[stage], empty[stage], acc_full[buf], acc_empty[buf]
+constexpr int kFull = 0, kEmpty = 4, kAccFull = 8, kAccEmpty = 10;
 
 struct GemmArgs {
   void* y;
@@ -45,18 +59,19 @@ struct GemmArgs {
   int32_t accumulate;   // kinds 0/1: Y += result
 };
 
-template <int KIND>
-__global__ void __launch_bounds__(192, 1)
+template <int KIND, int BM>
+__global__ void __launch_bounds__(GemmCfg<BM>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                 const __grid_constant__ GemmArgs g, unsigned int* err) {
+  using C = GemmCfg<BM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBarOff);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBarOff + 128);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kBarOff + 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles_m = (g.M + kBM - 1) / kBM;
+  const int tiles_m = (g.M + BM - 1) / BM;
   const int tiles_n = (g.N + kBN - 1) / kBN;
   const int tiles = tiles_m * tiles_n;
   const int kblocks = (g.K + kBK - 1) / kBK;
@@ -66,13 +81,13 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bar[kFull + i], 1);
       mbar_init(&bar[kEmpty + i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kBufs; ++i) {
       mbar_init(&bar[kAccFull + i], 1);
-      mbar_init(&bar[kAccEmpty + i], kEpiThreads);
+      mbar_init(&bar[kAccEmpty + i], 32 * C::kEpiWarps);
     }
     fence_mbar_init();
     tma_prefetch_desc(&mA);
@@ -88,25 +103,28 @@ __global__ void __launch_bounds__(192, 1)
     int it = 0;  // k-blocks issued over all tiles of this CTA
     bool ok = true;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-      const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
+      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * kBN;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const int st = it % kStages;
-        if (it >= kStages && !mbar_wait(&bar[kEmpty + st], ((it / kStages) - 1) & 1, err, 1501)) { ok = false; break; }
-        uint8_t* sA = sm + st * kStageBytes;
-        uint8_t* sB = sA + kABytes;
+        const int st = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&bar[kEmpty + st], ((it / C::kStages) - 1) & 1, err, 1501)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = sm + st * C::kStageBytes;
+        uint8_t* sB = sA + C::kABytes;
         const int k0 = kb * kBK;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&bar[kFull + st], kStageBytes);
+          mbar_arrive_expect_tx(&bar[kFull + st], C::kStageBytes);
           if (KIND == 2) {
-            // A[K,M]: two 64-wide M blocks of 64 K rows
-            for (int a = 0; a < kBM / 64; ++a) tma_load_2d(sA + a * 8192, &mA, &bar[kFull + st], m0 + a * 64, k0);
+            // A[K,M]: BM/64 blocks of 64 M columns x 64 K rows
+            for (int a = 0; a < BM / 64; ++a) tma_load_2d(sA + a * 8192, &mA, &bar[kFull + st], m0 + a * 64, k0);
           } else {
             tma_load_2d(sA, &mA, &bar[kFull + st], k0, m0);
           }
           if (KIND == 0) {
             tma_load_2d(sB, &mB, &bar[kFull + st], k0, n0);
           } else {
-            // B[K,N]: four 64-wide N blocks of 64 K rows
+            // B[K,N]: four blocks of 64 N columns x 64 K rows
             for (int a = 0; a < kBN / 64; ++a) tma_load_2d(sB + a * 8192, &mB, &bar[kFull + st], n0 + a * 64, k0);
           }
         }
@@ -114,30 +132,37 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     // every copy issued must land before the CTA exits
-    for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
-      mbar_wait(&bar[kFull + i % kStages], (i / kStages) & 1, err, 1502);
+    for (int i = (it > C::kStages ? it - C::kStages : 0); i < it; ++i)
+      mbar_wait(&bar[kFull + i % C::kStages], (i / C::kStages) & 1, err, 1502);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(kBM, kBN, KIND == 2, KIND >= 1);
+    constexpr uint32_t idesc = idesc_bf16(128, kBN, KIND == 2, KIND >= 1);
     int it = 0, local = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++local) {
-      const int buf = local & 1;
-      // the epilogue has drained this accumulator (two tiles ago)
-      if (local >= 2 && !mbar_wait(&bar[kAccEmpty + buf], ((local >> 1) - 1) & 1, err, 1503)) break;
+      const int buf = local % C::kBufs, use = local / C::kBufs;
+      // the epilogue has drained this accumulator (its previous tile)
+      if (use >= 1 && !mbar_wait(&bar[kAccEmpty + buf], (use - 1) & 1, err, 1503)) break;
       tc_fence_after();
-      const uint32_t acc = tmem + buf * kBN;
+      const uint32_t acc = tmem + buf * kBN;  // BM = 256: both halves, columns [0, 512)
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const int st = it % kStages;
-        if (!mbar_wait(&bar[kFull + st], (it / kStages) & 1, err, 1504)) { ok = false; break; }
+        const int st = it % C::kStages;
+        if (!mbar_wait(&bar[kFull + st], (it / C::kStages) & 1, err, 1504)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = smem_u32(sm + st * kStageBytes);
-        const uint32_t sB = sA + kABytes;
+        const uint32_t sA = smem_u32(sm + st * C::kStageBytes);
+        const uint32_t sB = sA + C::kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t da = KIND == 2 ? desc_mnmajor_sw128(sA + kk * 2048, 8192) : desc_kmajor_sw128(sA + kk * 32);
-          const uint64_t db = KIND == 0 ? desc_kmajor_sw128(sB + kk * 32) : desc_mnmajor_sw128(sB + kk * 2048, 8192);
-          if (elect_one()) mma_ss(acc, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int hm = 0; hm < BM / 128; ++hm) {
+          // rows 128*hm.. of the A tile into columns 256*hm.. of TMEM
+          const uint32_t sAh = sA + hm * 16384;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t da =
+                KIND == 2 ? desc_mnmajor_sw128(sAh + kk * 2048, 8192) : desc_kmajor_sw128(sAh + kk * 32);
+            const uint64_t db =
+                KIND == 0 ? desc_kmajor_sw128(sB + kk * 32) : desc_mnmajor_sw128(sB + kk * 2048, 8192);
+            if (elect_one()) mma_ss(acc + hm * kBN, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         if (elect_one()) mma_commit(&bar[kEmpty + st]);
         __syncwarp();
@@ -147,21 +172,23 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int part = (warp - 2) / 4;       // BM = 256: which 128-row half
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     int local = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
-      const int buf = local & 1;
-      const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
-      if (!mbar_wait(&bar[kAccFull + buf], (local >> 1) & 1, err, 1505)) break;
+      const int buf = local % C::kBufs, use = local / C::kBufs;
+      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * kBN;
+      if (!mbar_wait(&bar[kAccFull + buf], use & 1, err, 1505)) break;
       tc_fence_after();
-      const int row = m0 + quarter * 32 + lane;
+      const int row = m0 + part * 128 + quarter * 32 + lane;
+      const uint32_t col0 = (BM == 128 ? buf : part) * kBN;
       const bool row_ok = row < g.M && check(row >= 0, err, 1506);
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t r[32];
         __syncwarp();
-        tmem_ld32(tmem + lane_off + buf * kBN + c * 32, r);
+        tmem_ld32(tmem + lane_off + col0 + c * 32, r);
         tmem_ld_wait();
         const int col = n0 + c * 32;
         if (!row_ok || col >= g.N) {
@@ -217,21 +244,30 @@ int sm_count() {
   return n;
 }
 
-template <int KIND>
+// Tile height for a product: 256 rows when the output has enough 256 x 256
+// tiles to fill every SM at least twice, else 128 (more, smaller tiles).
+int tile_rows(int64_t M, int64_t N) {
+  const int64_t t256 = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
+  return t256 >= 2 * sm_count() ? 256 : 128;
+}
+
+template <int KIND, int BM>
 cudaError_t launch_kind(const CUtensorMap& mA, const CUtensorMap& mB, const GemmArgs& a, unsigned int* err,
                         cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  using C = GemmCfg<BM>;
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_kernel<KIND, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
+  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + kBN - 1) / kBN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  gemm_kernel<KIND><<<grid, 192, kSmemBytes, stream>>>(mA, mB, a, err);
+  gemm_kernel<KIND, BM><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, a, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // Row-major bf16 matrix [rows, cols] (cols contiguous) as a 2-D tensor map
-// with a box of box_cols x box_rows and 128-byte swizzle (box_cols = 64).
+// with a box of 64 columns (128 B, 128-byte swizzle) x box_rows.
 static bool map_2d(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, int box_rows) {
   return make_map_2d(m, p, rows, cols, 64, box_rows);
 }
@@ -239,30 +275,33 @@ static bool map_2d(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, in
 cudaError_t gemm_xwT(int64_t M, int N, int K, const void* X, const void* W, void* Y, bool accumulate,
                      unsigned int* err, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
+  const int bm = tile_rows(M, N);
   CUtensorMap mA, mB;
-  if (!map_2d(&mA, X, M, K, kBM) || !map_2d(&mB, W, N, K, kBN)) return cudaErrorInvalidValue;
+  if (!map_2d(&mA, X, M, K, bm) || !map_2d(&mB, W, N, K, kBN)) return cudaErrorInvalidValue;
   GemmArgs a{Y, static_cast<int32_t>(M), N, K, N, accumulate ? 1 : 0};
-  return launch_kind<0>(mA, mB, a, err, stream);
+  return bm == 256 ? launch_kind<0, 256>(mA, mB, a, err, stream) : launch_kind<0, 128>(mA, mB, a, err, stream);
 }
 
 cudaError_t gemm_dyW(int64_t M, int N, int K, const void* dY, const void* W, void* dX, unsigned int* err,
                      cudaStream_t stream) {
   // dX[M, N] = dY[M, K] . W[K, N]
   if (M == 0) return cudaSuccess;
+  const int bm = tile_rows(M, N);
   CUtensorMap mA, mB;
-  if (!map_2d(&mA, dY, M, K, kBM) || !map_2d(&mB, W, K, N, 64)) return cudaErrorInvalidValue;
+  if (!map_2d(&mA, dY, M, K, bm) || !map_2d(&mB, W, K, N, 64)) return cudaErrorInvalidValue;
   GemmArgs a{dX, static_cast<int32_t>(M), N, K, N, 0};
-  return launch_kind<1>(mA, mB, a, err, stream);
+  return bm == 256 ? launch_kind<1, 256>(mA, mB, a, err, stream) : launch_kind<1, 128>(mA, mB, a, err, stream);
 }
 
 cudaError_t gemm_dW(int M, int N, int64_t K, const void* dY, const void* X, float* dW, unsigned int* err,
                     cudaStream_t stream) {
   // dW[M, N] = dY[K, M]^T . X[K, N]
   if (K == 0) return cudaMemsetAsync(dW, 0, size_t(M) * N * 4, stream);
+  const int bm = tile_rows(M, N);
   CUtensorMap mA, mB;
   if (!map_2d(&mA, dY, K, M, 64) || !map_2d(&mB, X, K, N, 64)) return cudaErrorInvalidValue;
   GemmArgs a{dW, M, N, static_cast<int32_t>(K), N, 0};
-  return launch_kind<2>(mA, mB, a, err, stream);
+  return bm == 256 ? launch_kind<2, 256>(mA, mB, a, err, stream) : launch_kind<2, 128>(mA, mB, a, err, stream);
 }
 
 }  // namespace dkv

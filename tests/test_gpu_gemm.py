@@ -1,7 +1,9 @@
 """The layer's tensor-core GEMM (dualkv_gemm, csrc/gemm.cu) against fp64
 products of the same bf16 inputs (torch on the CPU), for its three operand
 layouts, with ragged tiles in every dimension, the residual add, K = 0, and
-two calls in a row on a persistent grid of more tiles than SMs.
+two calls in a row on a persistent grid of more tiles than SMs.  Outputs of
+more than two 256 x 256 tiles per SM take the 256-row tile kernel, smaller
+ones the 128-row kernel; both are covered.
 
 Bounds: bf16 results are one rounding of an fp32 sum, so rel-L2 <= 4e-3
 (the RMS relative error of bf16 rounding is about 1.1e-3); fp32 results
@@ -73,3 +75,30 @@ def test_many_tiles_twice_in_a_row():
     assert torch.equal(Y1, Y2)
     rows = torch.arange(0, M, 97)
     assert _rel(Y1[rows], A[rows].double() @ B.double().T) <= 4e-3
+
+
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_256_row_tiles_with_ragged_edges(kind):
+    """M = 19000, N = 2056: 675 tiles of 256 x 256, so the 256-row kernel runs,
+    with partial tiles at the M and N edges (and K not a multiple of 64)."""
+    from shared_prompt_exact_dualkv_gb300 import dualkv as D
+    M, N, K = 19000, 2056, 200
+    if kind == 0:
+        A, B = _bf16((M, K), 10), _bf16((N, K), 11)
+        ref = A.double() @ B.double().T
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    elif kind == 1:
+        A, B = _bf16((M, K), 12), _bf16((K, N), 13)
+        ref = A.double() @ B.double()
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    else:
+        A, B = _bf16((K, M), 14), _bf16((K, N), 15)
+        ref = A.double().T @ B.double()
+        Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    D.dualkv_gemm(kind, A.cuda(), B.cuda(), Y)
+    Y2 = Y.clone()
+    D.dualkv_gemm(kind, A.cuda(), B.cuda(), Y2)
+    assert D.dualkv_last_device_error()[0] == 0
+    assert torch.isfinite(Y.float()).all()
+    assert torch.equal(Y, Y2)
+    assert _rel(Y, ref) <= (1e-5 if kind == 2 else 4e-3)
