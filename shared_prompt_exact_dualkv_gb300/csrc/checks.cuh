@@ -41,19 +41,21 @@ struct RoleSteps {
   static constexpr int kRoles = 4;
 
   __device__ __forceinline__ void init() const {
-    if (kChecks)
+    if constexpr (kChecks) {
       for (int r = 0; r < kRoles; ++r) slot[r] = -1;
+    }
   }
   __device__ __forceinline__ void put(int role, int32_t steps) const {
-    if (kChecks) slot[role] = steps;
+    if constexpr (kChecks) slot[role] = steps;
   }
   // Every role that reported must have completed `expected` steps.  A role
   // that stopped early on a timed-out wait has already recorded that error,
   // which this one does not replace.
   __device__ __forceinline__ void verify(int32_t expected, unsigned int* err, uint32_t site) const {
-    if (!kChecks) return;
-    for (int r = 0; r < kRoles; ++r)
-      if (slot[r] != -1) check(slot[r] == expected, err, site);
+    if constexpr (kChecks) {
+      for (int r = 0; r < kRoles; ++r)
+        if (slot[r] != -1) check(slot[r] == expected, err, site);
+    }
   }
 };
 
