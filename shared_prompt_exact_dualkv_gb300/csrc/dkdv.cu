@@ -69,11 +69,22 @@ enum DkdvBar {
 };
 
 constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
-constexpr int kEwThreads = 256;  // elementwise threads (two per key row)
+// Each key row's 128 query columns are split over kColGroups elementwise
+// warps (the same TMEM lane quarter, different columns); the groups need no
+// exchange, the work being elementwise.
+constexpr int kColGroups = 2;
+constexpr int kCols = kTile / kColGroups;        // query columns per elementwise thread
+constexpr int kEwWarps = 4 * kColGroups;
+constexpr int kEwThreads = 32 * kEwWarps;
+constexpr int kThreads = kEwThreads + 64;        // + the copy producer and the MMA issuer
+constexpr int kProducerWarp = kEwWarps, kMmaWarp = kEwWarps + 1;
 
-// TMEM column offset of the K=16 slice kk of a bf16 operand stored as two
-// 32-column halves at +0 and +64 (queries 0..63 and 64..127).
-__device__ __forceinline__ uint32_t split_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+// TMEM column offset of the K=16 slice kk of a bf16 operand that each column
+// group g stored (packed two per column) at the start of its own range,
+// columns [g*kCols, g*kCols + kCols/2).
+__device__ __forceinline__ uint32_t split_col(int kk) {
+  return (16 * kk / kCols) * kCols + (16 * kk % kCols) / 2;
+}
 
 // The query tiles seen by one key-tile item, as "runs" of consecutive tiles
 // of one segment; the walk repeats the runs for each q-head of the group.
@@ -179,6 +190,28 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+// TMEM load of N (16, 32 or a multiple of 32) consecutive columns of this
+// warp's lanes, and store of N packed columns (16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  static_assert(N == 16 || N % 32 == 0, "TMEM load width");
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, r);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) tmem_ld32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+  static_assert(N == 16 || N == 32, "TMEM store width");
+  if constexpr (N == 16) {
+    tmem_st16(taddr, r);
+  } else {
+    tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(r));
+  }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -186,7 +219,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // dq_acc (FQ only): fp32 dQ accumulator [Hq][D/4][T][4] (unscaled); each
 // tile's dQ = dS K is added to it with fp32 vector reductions.
 template <int D, bool FQ>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Sched s, const __grid_constant__ CUtensorMap mQ,
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const __grid_constant__ CUtensorMap mdO, const float* __restrict__ lse,
@@ -215,11 +248,11 @@ __global__ void __launch_bounds__(320, 1)
   R.init(s, item, hk);
   const int n = R.per_head * R.group;
 
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 256) {
+  if (threadIdx.x == kEwThreads) {
     mbar_init(&bar[kKVFull], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kQFull + i], 2);
@@ -244,7 +277,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
     if (n > 0) {
       // (an out-of-range tile copy would only read zeros; the checks record it)
@@ -310,7 +343,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait(&bar[kQFull + (i & 1)], (i >> 1) & 1, err, 702);
       mbar_wait(&bar[kKVFull], 0, err, 703);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     // The warp runs the loop converged (warp-uniform control flow and
     // descriptors); one elected lane issues each MMA and commit.
@@ -401,10 +434,12 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ---------------------------------------------------------------- elementwise
+    constexpr int kDq = D / kColGroups;          // dQ / dK / dV columns per thread
+    constexpr int kCh = kDq < 32 ? kDq : 32;     // columns per TMEM load of those
     const int quarter = warp & 3;
-    const int half = warp >> 2;
+    const int grp = warp >> 2;                   // column group
     const int row = quarter * 32 + lane;
-    const int cb = half * 64;  // first query column of this thread
+    const int cb = grp * kCols;  // first query column of this thread
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = s.scale_log2;
     const bool key_in = R.k0 + row < R.k_end;
@@ -418,17 +453,16 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(&bar[kQFull + st], (i >> 1) & 1, err, 901)) { ok = false; break; }
         if (!mbar_wait(&bar[kSFull], i & 1, err, 902)) { ok = false; break; }
         tc_fence_after();
-        float p[64];
+        float p[kCols];
         {
-          uint32_t r[64];
-          tmem_ld32(tmem + lane_off + kColS + cb, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld32(tmem + lane_off + kColS + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          uint32_t r[kCols];
+          tmem_ld_cols<kCols>(tmem + lane_off + kColS + cb, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 64; ++u) p[u] = __uint_as_float(r[u]);
+          for (int u = 0; u < kCols; ++u) p[u] = __uint_as_float(r[u]);
         }
 #pragma unroll
-        for (int u = 0; u < 64; u += 4) {
+        for (int u = 0; u < kCols; u += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(vl + u);
           const float2 a0 = fma2(make_float2(p[u], p[u + 1]), make_float2(c, c), make_float2(-l4.x, -l4.y));
           const float2 a1 = fma2(make_float2(p[u + 2], p[u + 3]), make_float2(c, c), make_float2(-l4.z, -l4.w));
@@ -439,19 +473,19 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (it.diag()) {
 #pragma unroll
-          for (int u = 0; u < 64; ++u) p[u] = (cb + u < row) ? 0.f : p[u];
+          for (int u = 0; u < kCols; ++u) p[u] = (cb + u < row) ? 0.f : p[u];
         }
         if (FQ && !key_in) {
           // a key lane past the item's segment (the ragged end of a prompt
           // tile holds the first keys of the next segment) must not reach dQ
 #pragma unroll
-          for (int u = 0; u < 64; ++u) p[u] = 0.f;
+          for (int u = 0; u < kCols; ++u) p[u] = 0.f;
         }
         {
-          uint32_t pk[32];
+          uint32_t pk[kCols / 2];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
-          tmem_st32(tmem + lane_off + kColS + cb, pk);
+          for (int u = 0; u < kCols / 2; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
+          tmem_st_cols<kCols / 2>(tmem + lane_off + kColS + cb, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -460,7 +494,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(&bar[kdPFull], i & 1, err, 903)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int ci = 0; ci < 2; ++ci) {
+        for (int ci = 0; ci < kCols / 32; ++ci) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + kColdP + cb + ci * 32, r);
           tmem_ld_wait();
@@ -477,14 +511,16 @@ __global__ void __launch_bounds__(320, 1)
           if (!FQ) {
             tmem_st16(tmem + lane_off + kColdP + cb + ci * 16, pk);
           } else {
-            // row `row` (a key) of the query half `half`, 128-byte swizzled: the
-            // 16-byte chunk j of the row lands at chunk j ^ (row % 8).  The
-            // tile's previous contents were last read by the previous dK/dQ
-            // products, which completed before the previous drain.
-            const uint32_t rowb = smem_u32(sm + L::kdS + half * 16384 + row * 128);
+            // row `row` (a key) of its query columns cb.., 128-byte swizzled
+            // in the 64-query atom they fall in: the 16-byte chunk j of the
+            // row lands at chunk j ^ (row % 8).  The tile's previous contents
+            // were last read by the previous dK/dQ products, which completed
+            // before the previous drain.
+            const uint32_t rowb = smem_u32(sm + L::kdS + (cb / 64) * 16384 + row * 128);
+            const int ch0 = (cb % 64) / 8 + ci * 4;
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-              st_shared_v4(rowb + (((ci * 4 + v) ^ (row & 7)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              st_shared_v4(rowb + (((ch0 + v) ^ (row & 7)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
         if (!FQ) {
@@ -499,24 +535,22 @@ __global__ void __launch_bounds__(320, 1)
           // into the fp32 accumulator; the dP^T columns are then free again
           if (!mbar_wait(&bar[kdQFull], i & 1, err, 905)) { ok = false; break; }
           tc_fence_after();
-          uint32_t r[D / 2];
-#pragma unroll
-          for (int ci = 0; ci < D / 64; ++ci)
-            tmem_ld32(tmem + lane_off + kColdP + half * (D / 2) + ci * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[ci * 32]));
+          uint32_t r[kDq];
+          tmem_ld_cols<kDq>(tmem + lane_off + kColdP + grp * kDq, r);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bar[kdQFree]);
           const int q = it.q0() + row;
           const int h = it.head(R);
           if (q < it.seg_end && check(q >= 0 && q < s.T && h < s.Hq, err, 1108)) {
-            float* base = dq_acc + (static_cast<size_t>(h) * (D / 4) + half * (D / 8)) * s.T * 4 + static_cast<size_t>(q) * 4;
+            float* base = dq_acc + (static_cast<size_t>(h) * (D / 4) + grp * (kDq / 4)) * s.T * 4 + static_cast<size_t>(q) * 4;
 #pragma unroll
-            for (int v = 0; v < D / 8; ++v)
+            for (int v = 0; v < kDq / 4; ++v)
               red_add_v4(base + static_cast<size_t>(v) * s.T * 4, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
           }
         }
-        if (row == 0) steps.put(2 + half, i + 1);
+        if (row == 0 && (grp == 0 || grp == kColGroups - 1)) steps.put(2 + (grp ? 1 : 0), i + 1);
       }
     }
     // ---------------------------------------------------------------- epilogue
@@ -536,28 +570,28 @@ __global__ void __launch_bounds__(320, 1)
       const bool in_acc = !valid || check(R.acc0 + row < s.acc_rows && R.split < s.num_splits && hk < s.Hkv, err, 1104);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which ? kColdK : kColdV) + half * (D / 2);
+        const uint32_t col = (which ? kColdK : kColdV) + grp * kDq;
         const float mul = which ? s.scale : 1.f;
-        float* dst = (which ? pk_out : pv_out) + half * (D / 2);
+        float* dst = (which ? pk_out : pv_out) + grp * kDq;
 #pragma unroll
-        for (int ci = 0; ci < D / 64; ++ci) {
-          uint32_t r[32];
+        for (int ci = 0; ci < kDq / kCh; ++ci) {
+          uint32_t r[kCh];
           if (n > 0) {
-            tmem_ld32(tmem + lane_off + col + ci * 32, r);
+            tmem_ld_cols<kCh>(tmem + lane_off + col + ci * kCh, r);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) r[u] = 0u;
+            for (int u = 0; u < kCh; ++u) r[u] = 0u;
           }
           if (valid && in_acc && (ok || n == 0)) {
 #pragma unroll
-            for (int u = 0; u < 32; u += 4) {
+            for (int u = 0; u < kCh; u += 4) {
               const float a0 = __uint_as_float(r[u]) * mul, a1 = __uint_as_float(r[u + 1]) * mul;
               const float a2 = __uint_as_float(r[u + 2]) * mul, a3 = __uint_as_float(r[u + 3]) * mul;
               if (deterministic)
-                *reinterpret_cast<float4*>(dst + ci * 32 + u) = make_float4(a0, a1, a2, a3);
+                *reinterpret_cast<float4*>(dst + ci * kCh + u) = make_float4(a0, a1, a2, a3);
               else if (n > 0)
-                red_add_v4(dst + ci * 32 + u, a0, a1, a2, a3);
+                red_add_v4(dst + ci * kCh + u, a0, a1, a2, a3);
             }
           }
         }
@@ -566,22 +600,22 @@ __global__ void __launch_bounds__(320, 1)
       const size_t base = (static_cast<size_t>(k) * s.Hkv + hk) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which ? kColdK : kColdV) + half * (D / 2);
+        const uint32_t col = (which ? kColdK : kColdV) + grp * kDq;
         const float mul = which ? s.scale : 1.f;
-        uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + base + half * (D / 2));
+        uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + base + grp * kDq);
 #pragma unroll
-        for (int ci = 0; ci < D / 64; ++ci) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + col + ci * 32, r);
+        for (int ci = 0; ci < kDq / kCh; ++ci) {
+          uint32_t r[kCh];
+          tmem_ld_cols<kCh>(tmem + lane_off + col + ci * kCh, r);
           tmem_ld_wait();
-          uint32_t pk[16];
+          uint32_t pk[kCh / 2];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
+          for (int u = 0; u < kCh / 2; ++u)
             pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
           if (valid && check(k >= 0 && k < s.T && hk < s.Hkv, err, 1105)) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[ci * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < kCh / 8; ++v)
+              dst[ci * (kCh / 8) + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
       }
@@ -590,8 +624,8 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 256) steps.verify(n, err, 1106);
-  if (warp == 9) {
+  if (threadIdx.x == kEwThreads) steps.verify(n, err, 1106);
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -608,7 +642,7 @@ cudaError_t launch_dkdv_d(const Sched& s, const CUtensorMap& mQ, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, FQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(s.num_items) * static_cast<unsigned>(s.Hkv);
-  dkdv_kernel<D, FQ><<<grid, 320, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
+  dkdv_kernel<D, FQ><<<grid, kThreads, L::kBytes, stream>>>(s, mQ, mK, mV, mdO, lse, Dvec, static_cast<__nv_bfloat16*>(dk),
                                                        static_cast<__nv_bfloat16*>(dv), acc_k, acc_v, dq_acc,
                                                        deterministic, err);
   return cudaGetLastError();
