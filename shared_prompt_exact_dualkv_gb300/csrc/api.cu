@@ -143,29 +143,53 @@ void fill_common(Sched* s, const Shape& sh, float scale) {
   s->acc_rows = acc;
 }
 
+// One work item with its cost (tiles walked) and its locality set: the
+// items of one response segment read the same query (dK/dV) or key (forward,
+// dQ) tiles of that response; every other item is a set of its own.
 struct CostItem {
   int64_t cost;
   uint32_t item;
+  int32_t locality;
 };
 
+// Longest-first by locality set: sets in order of their longest item, a
+// set's items together, longest first.  The CTAs running at one time then
+// come from one response and read its tiles at about the same time, so L2
+// serves them once; listing items by cost alone interleaves all responses at
+// each cost, and each response's tiles come back from HBM once per cost
+// level.  Items in sets of their own keep the plain longest-first order.
 std::vector<uint32_t> sorted_items(std::vector<CostItem>& v) {
-  std::stable_sort(v.begin(), v.end(), [](const CostItem& a, const CostItem& b) { return a.cost > b.cost; });
+  std::vector<int64_t> gmax;
+  for (const CostItem& c : v) {
+    if (c.locality >= static_cast<int32_t>(gmax.size())) gmax.resize(c.locality + 1, 0);
+    gmax[c.locality] = std::max(gmax[c.locality], c.cost);
+  }
+  std::stable_sort(v.begin(), v.end(), [&](const CostItem& a, const CostItem& b) {
+    if (gmax[a.locality] != gmax[b.locality]) return gmax[a.locality] > gmax[b.locality];
+    if (a.locality != b.locality) return a.locality < b.locality;
+    return a.cost > b.cost;
+  });
   std::vector<uint32_t> out(v.size());
   for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].item;
   return out;
 }
 
 // Query-tile items (forward and dQ): cost = number of key tiles walked.
-// Prompt query tiles outside [pq_lo, pq_hi) are not listed.
+// Prompt query tiles outside [pq_lo, pq_hi) are not listed.  The query tiles
+// of one response form a locality set: they walk the same key tiles in the
+// same order.
 std::vector<uint32_t> query_items(const Sched& s) {
   std::vector<CostItem> v;
+  int32_t nloc = 0;
   for (int seg = 0; seg < s.nseg; ++seg) {
     const int p = s.prompt_of(seg);
     const int nt = s.seg_tiles(seg);
     const int nA = (p == seg) ? 0 : s.seg_tiles(p);
+    const int32_t g = nloc;
+    if (p != seg && nt > 0) ++nloc;
     for (int t = 0; t < nt; ++t) {
       if (p == seg && (t < s.pq_lo || t >= s.pq_hi)) continue;
-      v.push_back({nA + t + 1, make_item(t, seg, 0)});
+      v.push_back({nA + t + 1, make_item(t, seg, 0), p == seg ? nloc++ : g});
     }
   }
   return sorted_items(v);
@@ -180,11 +204,13 @@ std::vector<uint32_t> query_items(const Sched& s) {
 std::vector<uint32_t> key_items(const Sched& s, int S) {
   std::vector<uint32_t> out;
   std::vector<CostItem> v;
+  int32_t nloc = 0;
   for (int seg = 0; seg < s.nseg; ++seg) {
     if (s.prompt_of(seg) == seg && !v.empty()) {  // a new group starts
       const std::vector<uint32_t> g = sorted_items(v);
       out.insert(out.end(), g.begin(), g.end());
       v.clear();
+      nloc = 0;
     }
     const int nt = s.seg_tiles(seg);
     if (s.prompt_of(seg) == seg) {
@@ -197,10 +223,12 @@ std::vector<uint32_t> key_items(const Sched& s, int S) {
           // split 0 also walks the prompt's own query tiles j.. within [pq_lo, pq_hi)
           int64_t cost = (c == 0) ? std::max(0, std::min(nt, s.pq_hi) - std::max(j, s.pq_lo)) : 0;
           for (int i = seg + 1 + (c * ng) / S; i < seg + 1 + ((c + 1) * ng) / S; ++i) cost += s.seg_tiles(i);
-          v.push_back({cost, make_item(j, seg, c)});
+          v.push_back({cost, make_item(j, seg, c), nloc++});
         }
     } else {
-      for (int j = 0; j < nt; ++j) v.push_back({nt - j, make_item(j, seg, 0)});
+      // a response's key tiles read the same query tiles of that response
+      for (int j = 0; j < nt; ++j) v.push_back({nt - j, make_item(j, seg, 0), nloc});
+      ++nloc;
     }
   }
   const std::vector<uint32_t> g = sorted_items(v);

@@ -3,8 +3,10 @@
 // One CTA owns one 128-row key tile of one kv-head (and, for prompt key
 // tiles, one chunk of the N sequences).  It loops over every query tile that
 // sees those keys, for all q-heads of the kv-head's group (GQA):
-//   * a response key tile of sequence i: the later query tiles of response i
-//     (causal, the first one masked on the diagonal);
+//   * a response key tile of sequence i: the later query tiles of response i,
+//     from the last one down to the diagonal (masked causally), so the key
+//     tiles of one response, which run together, read the same query tile
+//     at about the same time;
 //   * a prompt key tile: the prompt's own later query tiles (split 0 only,
 //     causal) and every query tile of the responses in its chunk (no mask):
 //     the prompt keys are shared by all N sequences (DualKV research-map page,
@@ -127,13 +129,14 @@ struct QRuns {
   }
 };
 
-// Walk order of one key-tile item, per q-head of the group: the query tiles
-// of the responses in its chunk first, ascending, then (split 0 of a prompt
-// key tile) the prompt's own query tiles, descending from the last to the
-// key tile's diagonal.  Every prompt key tile of a group walks the responses
-// in the same order, so the CTAs that run together work on the same query
-// tiles at about the same time and L2 serves those tiles (and, with dQ fused,
-// takes their dQ reductions) for all of them.
+// Walk order of one key-tile item, per q-head of the group.  A prompt key
+// tile: the query tiles of the responses in its chunk first, ascending, then
+// (split 0) the prompt's own query tiles, descending from the last to the key
+// tile's diagonal.  A response key tile: its response's query tiles,
+// descending from the last to the diagonal.  The key tiles whose CTAs run
+// together (one group's prompt tiles, or one response's tiles) thus work on
+// the same query tiles at about the same time, and L2 serves those tiles
+// (and, with dQ fused, takes their dQ reductions) for all of them.
 struct QIter {
   int32_t hh, r, t, step, t_stop;   // t runs from its first tile by `step` until it reaches t_stop
   int32_t q_first, seg_end;
@@ -145,11 +148,18 @@ struct QIter {
     if (r < resp_runs(R)) {
       const int i = R.seq_lo + r;
       q_first = s.off[i];
-      t = R.prompt_item ? 0 : R.j;
-      t_stop = s.seg_tiles(i);
-      step = 1;
       seg_end = s.off[i + 1];
-      diag_t = R.prompt_item ? -1 : R.j;
+      if (R.prompt_item) {
+        t = 0;
+        t_stop = s.seg_tiles(i);
+        step = 1;
+        diag_t = -1;
+      } else {
+        t = s.seg_tiles(i) - 1;
+        t_stop = R.j - 1;
+        step = -1;
+        diag_t = R.j;
+      }
     } else {
       q_first = s.off[R.seg];
       t = min(R.nP, s.pq_hi) - 1;
