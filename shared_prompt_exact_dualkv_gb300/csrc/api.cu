@@ -42,6 +42,13 @@ int num_sms() {
   return n;
 }
 
+int l2_bytes() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 128 << 20;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 128 << 20;
+  return n;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
@@ -119,6 +126,7 @@ void fill_common(Sched* s, const Shape& sh, float scale) {
   s->scale_log2 = scale * 1.4426950408889634f;
   s->num_splits = 1;
   s->num_items = 0;
+  s->heads_outer = 0;
   s->pq_lo = 0;
   s->pq_hi = 0xFFFF;
   int seg = 0, r = 0;
@@ -172,6 +180,16 @@ std::vector<uint32_t> sorted_items(std::vector<CostItem>& v) {
   std::vector<uint32_t> out(v.size());
   for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].item;
   return out;
+}
+
+// Block order of the query-tile kernels.  Every response query tile walks its
+// prompt's keys and values; when those of all kv-heads exceed half of L2, the
+// CTAs running together should share one kv-head's, so the heads become the
+// outer block index.  Otherwise the items stay outer: the CTAs running
+// together then come from fewer responses and share those responses' tiles.
+int query_heads_outer(const Shape& sh) {
+  const int64_t prompt_kv = int64_t(sh.total_P) * sh.Hkv * sh.d * 2 * 2;
+  return prompt_kv > l2_bytes() / 2 ? 1 : 0;
 }
 
 // Query-tile items (forward and dQ): cost = number of key tiles walked.
@@ -412,6 +430,7 @@ int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float
   fill_common(s.get(), sh, scale);
   s->pq_lo = part.lo;
   s->pq_hi = part.hi;
+  s->heads_outer = query_heads_outer(sh);
   const std::vector<uint32_t> items = query_items(*s);
   CUtensorMap mQ, mK, mV;
   if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
@@ -459,6 +478,7 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   sk->num_splits = S;
   sq->pq_lo = sk->pq_lo = part.lo;
   sq->pq_hi = sk->pq_hi = part.hi;
+  sq->heads_outer = query_heads_outer(sh);
   const std::vector<uint32_t> q_items = query_items(*sq);
   const std::vector<uint32_t> k_items = key_items(*sk, S);
   std::unique_ptr<PromptMap> map(make_prompt_map(sh));

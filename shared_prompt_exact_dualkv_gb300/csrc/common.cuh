@@ -36,6 +36,8 @@ struct Sched {
   int32_t acc_rows;                 // prompt rows in all groups (fp32 accumulator rows)
   float scale;                      // softmax scale
   float scale_log2;                 // softmax scale * log2(e)
+  int32_t heads_outer;              // query-tile kernels: block b is head b / num_items, item b % num_items
+                                    // (0: item b / heads, head b % heads)
   int32_t pq_lo, pq_hi;             // prompt query tiles [pq_lo, pq_hi) of every prompt take part
                                     // (0, 0xFFFF = all; a rank of a sharded step takes a part)
   int32_t off[kMaxSeg + 1];         // segment s is packed rows [off[s], off[s+1])

@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t item = s.items[blockIdx.x / s.Hq];
-  const int h = blockIdx.x % s.Hq;
+  const uint32_t item = s.items[s.heads_outer ? blockIdx.x % s.num_items : blockIdx.x / s.Hq];
+  const int h = s.heads_outer ? blockIdx.x / s.num_items : blockIdx.x % s.Hq;
   const int hk = h / s.group;
   KeyWalk w;
   w.init(s, item);

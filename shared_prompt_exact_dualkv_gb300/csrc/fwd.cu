@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int slots = fwd_head_slots(s.Hq, s.group);
-  const uint32_t item = s.items[blockIdx.x / slots];
-  const int slot = blockIdx.x % slots;
+  const uint32_t item = s.items[s.heads_outer ? blockIdx.x % s.num_items : blockIdx.x / slots];
+  const int slot = s.heads_outer ? blockIdx.x / s.num_items : blockIdx.x % slots;
   const bool paired = (s.group % 2 == 0);
   const int nheads = paired ? 2 : 1;
   const int h0 = paired ? 2 * slot : slot;  // head A; head B = h0 + 1

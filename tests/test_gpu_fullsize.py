@@ -135,3 +135,34 @@ def test_fullsize_parity(name):
     for x_, y_ in zip(grads[False], grads[True]):
         diff = float(torch.linalg.vector_norm(x_.float() - y_.float()) / torch.linalg.vector_norm(y_.float()))
         assert diff <= 3e-3, diff
+
+
+def test_head_outer_block_order_parity():
+    """The forward and dQ kernels take the heads as the outer block index when
+    the prompt's keys and values of all kv-heads exceed half of L2 (P32K and
+    P64K do).  Here with a ragged prompt tail, a ragged last response and an
+    empty one: every row of the first and last kv-head groups against the
+    oracle, both dK/dV modes."""
+    from shared_prompt_exact_dualkv_gb300 import dualkv as D
+    torch.set_num_threads(os.cpu_count() or 1)
+    w = synthetic.make_workload("head_outer", 16, 8, 128, 24001, (300, 1000, 0, 129))
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    assert w.P * w.Hkv * w.d * 4 > l2 // 2, "the case must take the head-outer order"
+    g = w.Hq // w.Hkv
+    x = synthetic.make_inputs(w, seed=3)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.dout))
+    out, lse = D.forward(q, k, v, w.P, w.R_lens, w.scale)
+    grads = {det: D.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale, deterministic=det)
+             for det in (False, True)}
+    st, site = D.dualkv_last_device_error()
+    assert st == 0, (st, site)
+    for kvh in (0, w.Hkv - 1):
+        hs = slice(kvh * g, (kvh + 1) * g)
+        ref = okg.kvgroup_forward_backward(*_group_inputs(x, w, kvh), w.P, w.R_lens, w.scale)
+        tag = f"head-outer kv-head {kvh}"
+        _check(tag + " out", _cpu(out[:, hs]), ref["out"].numpy(), "out")
+        _check(tag + " lse", lse[hs].cpu().double().numpy(), ref["lse"].numpy(), "lse")
+        for det, (dq, dk, dv) in grads.items():
+            _check(f"{tag} det={det} dq", _cpu(dq[:, hs]), ref["dq"].numpy(), "grad")
+            _check(f"{tag} det={det} dk", _cpu(dk[:, kvh]), ref["dk"].numpy(), "grad")
+            _check(f"{tag} det={det} dv", _cpu(dv[:, kvh]), ref["dv"].numpy(), "grad")
