@@ -206,13 +206,18 @@ def recorded_traffic(kernel: str, workload: str, deterministic: bool):
 def end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world):
     """Same step through the C ABI with host buffers: every step copies its
     inputs from pinned host memory and its results (out, lse, dq, dk, dv) back.
-    Two device buffer sets let step k+1's host-to-device copies (copy-in
-    stream) and step k-1's device-to-host copies (copy-out stream) overlap
-    step k's kernels.  Returns (ms per step, h2d bytes, d2h bytes)."""
+    A ring of `args.e2e_buffers` device buffer sets lets the host-to-device
+    copies (copy-in stream) run up to that many steps minus one ahead of the
+    kernels, and the device-to-host copies (copy-out stream) trail them.  Two
+    sets suffice while every copy runs at link speed; a deeper ring keeps the
+    kernels fed through the occasional single copy that stalls for about
+    100 ms on these hosts after sustained load.  Returns (ms per step, h2d
+    bytes, d2h bytes)."""
+    nb = max(2, args.e2e_buffers)
     hin = [t.pin_memory() for t in (x.q, x.k, x.v, x.dout)]
     h2d = sum(t.numel() * t.element_size() for t in hin)
     bufs = []
-    for b in range(2):
+    for b in range(nb):
         ins = [torch.empty_like(t, device=dev) for t in (x.q, x.k, x.v, x.dout)]
         outs = [torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
                 torch.empty_like(v)]
@@ -221,21 +226,21 @@ def end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world):
         bufs.append((ins, outs, hout, bws))
     d2h = sum(t.numel() * t.element_size() for t in bufs[0][2])
     cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in_ready", "comp_done", "out_done")}
+    ev = {name: [torch.cuda.Event() for _ in range(nb)] for name in ("in_ready", "comp_done", "out_done")}
 
     def e2e_step(i):
-        b = i & 1
+        b = i % nb
         ins, outs, hout, bws = bufs[b]
         (eq, ek, ev_, edo), (eo, el, edq, edk, edv) = ins, outs
         with torch.cuda.stream(cin):
-            if i >= 2:
-                cin.wait_event(ev["comp_done"][b])   # step i-2 finished reading this input set
+            if i >= nb:
+                cin.wait_event(ev["comp_done"][b])   # step i-nb finished reading this input set
             for dst, src in zip(ins, hin):
                 dst.copy_(src, non_blocking=True)
             ev["in_ready"][b].record(cin)
         stream.wait_event(ev["in_ready"][b])
-        if i >= 2:
-            stream.wait_event(ev["out_done"][b])     # step i-2's results have left this output set
+        if i >= nb:
+            stream.wait_event(ev["out_done"][b])     # step i-nb's results have left this output set
         D.dualkv_fwd(eq, ek, ev_, w.P, w.R_lens, eo, el, w.scale, stream)
         D.dualkv_bwd(eq, ek, ev_, eo, edo, el, w.P, w.R_lens, w.scale, det, bws, edq, edk, edv, stream=stream)
         ev["comp_done"][b].record(stream)
@@ -245,7 +250,7 @@ def end_to_end(args, D, w, x, dev, q, lse, k, v, ws, stream, det, world):
                 dst.copy_(src, non_blocking=True)
             ev["out_done"][b].record(cout)
 
-    for i in range(2):
+    for i in range(nb):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
@@ -587,6 +592,8 @@ def main():
                          "workload's packed rows")
     ap.add_argument("--groups", action="store_true",
                     help="also time four prompt groups in one call against four single-group calls")
+    ap.add_argument("--e2e-buffers", type=int, default=3,
+                    help="device buffer sets in the end-to-end leg's copy/compute ring (at least 2)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="also skip the end-to-end leg (for profiling: one buffer set on the device)")
     args = ap.parse_args()
@@ -659,7 +666,7 @@ def main():
     if e2e is not None:
         e2e_ms, h2d, d2h = e2e
         e2e_obj = {"value": weak_scaling_value(flops, e2e_ms, world), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "buffer_sets": max(2, args.e2e_buffers)}
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
