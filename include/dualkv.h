@@ -268,6 +268,15 @@ DUALKV_API int dualkv_selftest_wait_timeout(int64_t limit_ns, int32_t site, void
 DUALKV_API const char* dualkv_status_string(int status);
 
 /*
+ * The CUDA code behind the calling thread's most recent DUALKV_ERR_CUDA from
+ * any entry point of this library: a cudaError_t value, or, where a tensor
+ * map was rejected, the driver's CUresult (-1 if the encoder could not be
+ * reached).  0 if the thread has had no such failure.  Not reset by
+ * successful calls.
+ */
+DUALKV_API int32_t dualkv_last_cuda_error(void);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns DUALKV_OK, DUALKV_ERR_TIMEOUT (a bounded device wait gave
  * up; *site, if non-NULL, receives the kernel-specific wait site id),

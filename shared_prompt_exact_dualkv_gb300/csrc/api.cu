@@ -330,7 +330,7 @@ cudaError_t launch_chunks(Sched* s, const std::vector<uint32_t>& items, F&& laun
   return cudaSuccess;
 }
 
-int map_cuda(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : DUALKV_ERR_CUDA; }
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : cuda_fail(e); }
 
 // ------------------------------------------------------------------ tracing
 constexpr int kTraceKernels = 5;
@@ -435,9 +435,9 @@ int fwd_impl(const Shape& sh, const void* q, const void* k, const void* v, float
   CUtensorMap mQ, mK, mV;
   if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
       !make_map_thd(&mV, v, sh.T, sh.Hkv, sh.d, kTile))
-    return DUALKV_ERR_CUDA;
+    return cuda_fail(last_map_result());
   unsigned int* err = error_word_ptr();
-  if (!err) return DUALKV_ERR_CUDA;
+  if (!err) return cuda_fail(cudaGetLastError());
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return map_cuda(launch_chunks(s.get(), items, [&](const Sched& c) {
     TraceScope ts(0, cs);
@@ -485,9 +485,9 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
   CUtensorMap mQ, mK, mV, mdO;
   if (!make_map_thd(&mQ, q, sh.T, sh.Hq, sh.d, kTile) || !make_map_thd(&mK, k, sh.T, sh.Hkv, sh.d, kTile) ||
       !make_map_thd(&mV, v, sh.T, sh.Hkv, sh.d, kTile) || !make_map_thd(&mdO, dout, sh.T, sh.Hq, sh.d, kTile))
-    return DUALKV_ERR_CUDA;
+    return cuda_fail(last_map_result());
   unsigned int* err = error_word_ptr();
-  if (!err) return DUALKV_ERR_CUDA;
+  if (!err) return cuda_fail(cudaGetLastError());
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* wb = static_cast<uint8_t*>(workspace);
   float* Dvec = reinterpret_cast<float*>(wb + ws.D);
@@ -533,6 +533,17 @@ int bwd_impl(const Shape& sh, const void* q, const void* k, const void* v, const
 }  // namespace
 
 unsigned int* device_error_word() { return error_word_ptr(); }
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+}
+
+int cuda_fail(int code) {
+  t_last_cuda_error = code;
+  return DUALKV_ERR_CUDA;
+}
+
+int last_cuda_error() { return t_last_cuda_error; }
 
 }  // namespace dkv
 
@@ -668,8 +679,9 @@ int dualkv_trace_read(double* ms, int64_t* launches, int32_t n) {
   int status = DUALKV_OK;
   for (auto& r : t.pending) {
     float el = 0.f;
-    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&el, r.a, r.b) != cudaSuccess)
-      status = DUALKV_ERR_CUDA;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&el, r.a, r.b);
+    if (e != cudaSuccess) status = cuda_fail(e);
     t.ms[r.kernel] += el;
     t.launches[r.kernel] += 1;
     t.pool.push_back(r.a);
@@ -683,22 +695,25 @@ int dualkv_trace_read(double* ms, int64_t* launches, int32_t n) {
   return status;
 }
 
+int32_t dualkv_last_cuda_error(void) { return last_cuda_error(); }
+
 int dualkv_selftest_wait_timeout(int64_t limit_ns, int32_t site, void* stream) {
   if (limit_ns < 1 || limit_ns > 10000000000ll || site < 1 || site > 0xFFFFFF) return DUALKV_ERR_INVALID_ARG;
   unsigned int* err = error_word_ptr();
-  if (!err) return DUALKV_ERR_CUDA;
+  if (!err) return cuda_fail(cudaGetLastError());
   return map_cuda(launch_wait_timeout_selftest(err, static_cast<uint64_t>(limit_ns), static_cast<uint32_t>(site),
                                                static_cast<cudaStream_t>(stream)));
 }
 
 int dualkv_last_device_error(void* stream, int32_t* site) {
   if (site) *site = 0;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   unsigned int w = 0;
-  if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if ((e = cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w))) != cudaSuccess) return cuda_fail(e);
   if (w == 0) return DUALKV_OK;
   const unsigned int zero = 0;
-  if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if ((e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
   if (site) *site = static_cast<int32_t>(w >> 8);
   const int kind = static_cast<int>(w & 0xFFu);
   return (kind == DUALKV_ERR_TIMEOUT || kind == DUALKV_ERR_CHECK) ? kind : DUALKV_ERR_CUDA;
@@ -739,7 +754,7 @@ int dualkv_bwd_static_workspace(const void* q, const void* k, const void* v, con
   const size_t need = dualkv_bwd_workspace_bytes(P, N, R_lens, Hq, Hkv, d, deterministic, num_splits);
   if (need > DUALKV_STATIC_SCRATCH_BYTES) return DUALKV_ERR_WORKSPACE;
   void* ws = static_scratch_device_ptr();
-  if (!ws) return DUALKV_ERR_CUDA;
+  if (!ws) return cuda_fail(cudaGetLastError());
   return dualkv_bwd(q, k, v, out, dout, lse, P, N, R_lens, Hq, Hkv, d, softmax_scale, deterministic, num_splits,
                     ws, DUALKV_STATIC_SCRATCH_BYTES, dq, dk, dv, stream);
 }

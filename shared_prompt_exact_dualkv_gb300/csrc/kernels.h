@@ -64,6 +64,13 @@ cudaError_t launch_prompt_reduce(const float* src_k, const float* src_v, int nsp
 // up once per device), or null.
 unsigned int* device_error_word();
 
+// Records the CUDA code behind a failure (a cudaError_t, or the driver result
+// of a rejected tensor map) for the calling thread's dualkv_last_cuda_error
+// and returns DUALKV_ERR_CUDA.
+int cuda_fail(int code);
+inline int cuda_fail(cudaError_t e) { return cuda_fail(static_cast<int>(e)); }
+int last_cuda_error();
+
 // Self-test of the bounded waits: a wait on an mbarrier phase that never
 // completes gives up after limit_ns and records a timeout at `site`.
 cudaError_t launch_wait_timeout_selftest(unsigned int* err, uint64_t limit_ns, uint32_t site, cudaStream_t stream);

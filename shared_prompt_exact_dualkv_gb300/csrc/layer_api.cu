@@ -130,26 +130,28 @@ size_t attention_ws_bytes(const dualkv_layer_config& c, int32_t G, const int64_t
 struct Gemm {
   cudaStream_t stream = nullptr;
   unsigned int* err = nullptr;
-  bool ok = true;
+  cudaError_t e = cudaSuccess;
 
+  bool ok() const { return e == cudaSuccess; }
+  int status() const { return ok() ? DUALKV_OK : cuda_fail(e); }
   // Y[rows, out] (+)= X[rows, in] . W[out, in]^T
   void xwT(int64_t rows, int out, int in, const void* X, const void* W, void* Y, float beta) {
-    if (ok) ok = gemm_xwT(rows, out, in, X, W, Y, beta != 0.f, err, stream) == cudaSuccess;
+    if (ok()) e = gemm_xwT(rows, out, in, X, W, Y, beta != 0.f, err, stream);
   }
   // dX[rows, in] = dY[rows, out] . W[out, in]
   void dyW(int64_t rows, int out, int in, const void* dY, const void* W, void* dX) {
-    if (ok) ok = gemm_dyW(rows, in, out, dY, W, dX, err, stream) == cudaSuccess;
+    if (ok()) e = gemm_dyW(rows, in, out, dY, W, dX, err, stream);
   }
   // dW[out, in] (fp32) = dY[rows, out]^T . X[rows, in]
   void dW(int64_t rows, int out, int in, const void* dY, const void* X, float* dWp) {
-    if (ok) ok = gemm_dW(out, in, rows, dY, X, dWp, err, stream) == cudaSuccess;
+    if (ok()) e = gemm_dW(out, in, rows, dY, X, dWp, err, stream);
   }
 };
 
 int begin_gemms(Gemm* g, cudaStream_t st) {
   g->stream = st;
   g->err = device_error_word();
-  return g->err ? DUALKV_OK : DUALKV_ERR_CUDA;
+  return g->err ? DUALKV_OK : cuda_fail(cudaGetLastError());
 }
 
 int weights_ok(const dualkv_layer_weights* w) {
@@ -160,7 +162,7 @@ int weights_ok(const dualkv_layer_weights* w) {
   return DUALKV_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : DUALKV_ERR_CUDA; }
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DUALKV_OK : cuda_fail(e); }
 
 }  // namespace
 }  // namespace dkv
@@ -221,30 +223,30 @@ int dualkv_layer_fwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   if ((st = begin_gemms(&gm, cs)) != DUALKV_OK) return st;
 
   cudaError_t e = launch_rmsnorm_fwd(x, w->ln1, ws + L.h1, reinterpret_cast<float*>(ws + L.r1), T, H, c.eps, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   gm.xwT(T, nq + 2 * nk, H, ws + L.h1, w->wqkv, ws + L.qkv, 0.f);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   e = launch_rope_split(*map, ws + L.qkv, ws + L.q, ws + L.k, ws + L.v, static_cast<int>(T), c.Hq, c.Hkv, c.d,
                         c.rope_base, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   st = dualkv_fwd_groups(ws + L.q, ws + L.k, ws + L.v, G, P, N, R_lens, c.Hq, c.Hkv, c.d,
                          1.f / std::sqrt(static_cast<float>(c.d)), ws + L.a, reinterpret_cast<float*>(ws + L.lse),
                          stream);
   if (st != DUALKV_OK) return st;
-  if (cudaMemcpyAsync(ws + L.x2, x, size_t(T) * H * 2, cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
-    return DUALKV_ERR_CUDA;
+  if ((e = cudaMemcpyAsync(ws + L.x2, x, size_t(T) * H * 2, cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+    return cuda_fail(e);
   gm.xwT(T, H, nq, ws + L.a, w->wo, ws + L.x2, 1.f);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   e = launch_rmsnorm_fwd(ws + L.x2, w->ln2, ws + L.h2, reinterpret_cast<float*>(ws + L.r2), T, H, c.eps, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   gm.xwT(T, 2 * I, H, ws + L.h2, w->wgu, ws + L.gu, 0.f);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   e = launch_swiglu_fwd(ws + L.gu, ws + L.m, T, I, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
-  if (cudaMemcpyAsync(y, ws + L.x2, size_t(T) * H * 2, cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
-    return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpyAsync(y, ws + L.x2, size_t(T) * H * 2, cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+    return cuda_fail(e);
   gm.xwT(T, H, I, ws + L.m, w->wd, y, 1.f);
-  return gm.ok ? DUALKV_OK : DUALKV_ERR_CUDA;
+  return gm.status();
 }
 
 int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_layer_weights* w, const void* x, const void* dy,
@@ -283,20 +285,20 @@ int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   // MLP: dWd, dm (over m), dgu (over gu), dWgu, dh2
   gm.dW(T, H, I, dy, ws + L.m, grads->wd);
   gm.dyW(T, H, I, dy, w->wd, ws + L.m);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   cudaError_t e = launch_swiglu_bwd(ws + L.gu, ws + L.m, ws + L.gu, T, I, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   gm.dW(T, 2 * I, H, ws + L.gu, ws + L.h2, grads->wgu);
   gm.dyW(T, 2 * I, H, ws + L.gu, w->wgu, ws + L.dh2);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   // second norm, with the residual path: dx2 = dy + RMSNorm'(dh2)
   e = launch_rmsnorm_bwd(ws + L.dh2, ws + L.x2, w->ln2, reinterpret_cast<const float*>(ws + L.r2), dy, ws + L.dx2,
                          reinterpret_cast<float*>(ws + L.part), grads->ln2, T, H, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   // attention output projection
   gm.dW(T, H, nq, ws + L.dx2, ws + L.a, grads->wo);
   gm.dyW(T, H, nq, ws + L.dx2, w->wo, ws + L.da);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   if (T > 0) {
     st = dualkv_bwd_groups(ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.da, reinterpret_cast<const float*>(ws + L.lse),
                            G, P, N, R_lens, c.Hq, c.Hkv, c.d, 1.f / std::sqrt(static_cast<float>(c.d)), 0, 0,
@@ -305,10 +307,10 @@ int dualkv_layer_bwd(const dualkv_layer_config* cfg, const dualkv_layer_weights*
   }
   e = launch_rope_merge(*map, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.qkv, static_cast<int>(T), c.Hq, c.Hkv, c.d,
                         c.rope_base, cs);
-  if (e != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   gm.dW(T, nq + 2 * nk, H, ws + L.qkv, ws + L.h1, grads->wqkv);
   gm.dyW(T, nq + 2 * nk, H, ws + L.qkv, w->wqkv, ws + L.dh1);
-  if (!gm.ok) return DUALKV_ERR_CUDA;
+  if (!gm.ok()) return gm.status();
   // first norm: dx = dx2 + RMSNorm'(dh1)
   e = launch_rmsnorm_bwd(ws + L.dh1, x, w->ln1, reinterpret_cast<const float*>(ws + L.r1), ws + L.dx2, dx,
                          reinterpret_cast<float*>(ws + L.part), grads->ln1, T, H, cs);
@@ -327,7 +329,7 @@ int dualkv_gemm(int32_t kind, int64_t M, int64_t N, int64_t K, const void* A, co
   if (!Y || (K > 0 && (!A || !B))) return DUALKV_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(Y)) return DUALKV_ERR_ALIGNMENT;
   unsigned int* err = device_error_word();
-  if (!err) return DUALKV_ERR_CUDA;
+  if (!err) return cuda_fail(cudaGetLastError());
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (kind == 0) {

@@ -26,6 +26,27 @@ inline EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+// The encoder is a driver call and needs a current context on the calling
+// thread.  A thread whose first CUDA work this is (an autograd worker thread,
+// say) has none until a runtime call binds the device's primary context,
+// which cudaSetDevice does.
+inline bool bind_primary_context() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
+}
+
+// The driver's result for the calling thread's last rejected tensor map
+// (-1: no encoder, no context or invalid arguments).
+inline int& last_map_result() {
+  static thread_local int r = 0;
+  return r;
+}
+
+inline bool encode_failed(int r) {
+  last_map_result() = r;
+  return false;
+}
+
 // Tensor map over a row-major [T, H, d] bf16 tensor (token, head, feature).
 // One box is 64 features (128 B, one swizzle row) x 1 head x `box_rows`
 // tokens, landing in shared memory as `box_rows` 128-byte rows with the
@@ -33,7 +54,7 @@ inline EncodeTiledFn encode_tiled_fn() {
 // Returns false if the driver rejects the map.
 inline bool make_map_thd(CUtensorMap* m, const void* base, int64_t T, int H, int d, int box_rows) {
   EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn) return false;
+  if (!fn || !bind_primary_context()) return encode_failed(-1);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
@@ -42,7 +63,7 @@ inline bool make_map_thd(CUtensorMap* m, const void* base, int64_t T, int H, int
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return r == CUDA_SUCCESS || encode_failed(static_cast<int>(r));
 }
 
 // Tensor map over a row-major [rows, cols] bf16 matrix (cols contiguous, a
@@ -51,7 +72,7 @@ inline bool make_map_thd(CUtensorMap* m, const void* base, int64_t T, int H, int
 // Elements past either extent read as zero.
 inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
   EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn || rows < 1 || cols < 1 || cols % 8 != 0) return false;
+  if (!fn || rows < 1 || cols < 1 || cols % 8 != 0 || !bind_primary_context()) return encode_failed(-1);
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
@@ -59,7 +80,7 @@ inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t 
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return r == CUDA_SUCCESS || encode_failed(static_cast<int>(r));
 }
 
 }  // namespace dkv

@@ -32,7 +32,7 @@ EXPORTED = ("dualkv_fwd", "dualkv_bwd", "dualkv_bwd_workspace_bytes", "dualkv_st
             "dualkv_bwd_static_workspace", "dualkv_fwd_groups", "dualkv_bwd_groups_workspace_bytes",
             "dualkv_bwd_groups", "dualkv_layer_workspace_bytes", "dualkv_layer_fwd", "dualkv_layer_bwd",
             "dualkv_packed_positions", "dualkv_selftest_wait_timeout", "dualkv_fwd_partial", "dualkv_bwd_partial",
-            "dualkv_checks_enabled", "dualkv_gemm")
+            "dualkv_checks_enabled", "dualkv_gemm", "dualkv_last_cuda_error")
 
 # Size of the library's fixed backward scratch (DUALKV_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -75,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.dualkv_bwd.restype = ctypes.c_int
     lib.dualkv_status_string.argtypes = [ctypes.c_int]
     lib.dualkv_status_string.restype = ctypes.c_char_p
+    lib.dualkv_last_cuda_error.argtypes = []
+    lib.dualkv_last_cuda_error.restype = c_i32
     lib.dualkv_last_device_error.argtypes = [c_p, p_i32]
     lib.dualkv_last_device_error.restype = ctypes.c_int
     lib.dualkv_trace_enable.argtypes = [ctypes.c_int]
@@ -129,7 +131,14 @@ lib = _load()
 class DualKVError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {dualkv_status_string(status)} (status {status})")
+        self.cuda_error = dualkv_last_cuda_error() if status == DUALKV_ERR_CUDA else 0
+        detail = f", CUDA code {self.cuda_error}" if self.cuda_error else ""
+        super().__init__(f"{where}: {dualkv_status_string(status)} (status {status}{detail})")
+
+
+def dualkv_last_cuda_error() -> int:
+    """The CUDA code behind this thread's most recent DUALKV_ERR_CUDA (0: none)."""
+    return int(lib.dualkv_last_cuda_error())
 
 
 def dualkv_status_string(status: int) -> str:

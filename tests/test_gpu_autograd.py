@@ -26,3 +26,46 @@ def test_autograd_matches_direct_calls(groups):
     rdq, rdk, rdv = D.backward_groups(q, k, v, ref_out, do, lse, groups, deterministic=True, num_splits=2)
     assert torch.equal(out.detach(), ref_out)
     assert torch.equal(qa.grad, rdq) and torch.equal(ka.grad, rdk) and torch.equal(va.grad, rdv)
+
+
+def test_calls_from_new_host_threads():
+    """Library calls from threads whose first CUDA work they are (the
+    autograd engine runs backward on such a worker thread).  The tensor-map
+    encoder is a driver call that needs a current context, which the library
+    binds itself.  Each thread's results equal the main thread's bit for bit
+    (deterministic mode)."""
+    import threading
+    from shared_prompt_exact_dualkv_gb300 import dualkv as D
+    P, R = 300, (200, 0, 131)
+    x = synthetic.draw_inputs(P + sum(R), 4, 2, 128, 5)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.dout))
+    out, lse = D.forward(q, k, v, P, R)
+    ref = D.backward(q, k, v, out, do, lse, P, R, deterministic=True)
+    torch.cuda.synchronize()
+    results, errors = [], []
+
+    def work():
+        try:
+            o, l = D.forward(q, k, v, P, R)
+            g = D.backward(q, k, v, o, do, l, P, R, deterministic=True)
+            torch.cuda.synchronize()
+            results.append((o, l) + tuple(g))
+        except Exception as e:   # reported below, in the test's thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work) for _ in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for r in results:
+        for a, b in zip(r, (out, lse) + tuple(ref)):
+            assert torch.equal(a, b)
+
+
+def test_autograd_after_other_library_work():
+    """The autograd case again, after the library has run in the main thread
+    (the order in which the worker thread first met a missing context)."""
+    test_calls_from_new_host_threads()
+    test_autograd_matches_direct_calls([(300, (200, 0, 131))])
