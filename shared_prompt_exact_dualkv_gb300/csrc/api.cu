@@ -1,5 +1,6 @@
-// C ABI (include/dualkv.h): argument checks, the longest-first tile
-// schedules, TMA tensor maps, workspace layout and the launch sequence.
+// C ABI (include/dualkv.h): argument checks, the tile schedules (longest
+// first, each response's items together), TMA tensor maps, workspace layout
+// and the launch sequence.
 #include <algorithm>
 #include <cmath>
 #include <cstring>

@@ -4,7 +4,8 @@
 // is its prompt followed by its N responses; a launch may hold several
 // groups (micro-batches of several prompts, research-map page "Key
 // results": mb=8).  Work is cut into 128-row tiles that never straddle a
-// segment; the host lists them longest-first in the launch parameters.
+// segment; the host lists them longest-first (each response's items
+// together) in the launch parameters.
 #pragma once
 
 #include <cstdint>
