@@ -83,6 +83,25 @@ def main():
     print(json.dumps({"case": "partial", "dq": rel(dq[128:], rq[128:]), "dk": rel(dk, rk), "dv": rel(dv, rv),
                       "dk_prompt_f32": rel(f32[1], rk[:w.P]), "status": st, "site": site}), flush=True)
 
+    # a prompt whose keys and values exceed half of L2: the forward and dQ
+    # blocks take the heads as their outer index; kv-head 0 against the
+    # kv-group oracle (torch fp64)
+    from oracle import kvgroup as okg
+    w = synthetic.make_workload("head_outer", 8, 8, 128, 20000, (129, 300))
+    assert w.P * w.Hkv * w.d * 4 > torch.cuda.get_device_properties(0).L2_cache_size // 2
+    x = synthetic.make_inputs(w, seed=7)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.dout))
+    out, lse = D.forward(q, k, v, w.P, w.R_lens, w.scale)
+    g = D.backward(q, k, v, out, do, lse, w.P, w.R_lens, w.scale)
+    st, site = D.dualkv_last_device_error()
+    f64 = lambda t: t.to(torch.float64).contiguous()
+    ref = okg.kvgroup_forward_backward(f64(x.q[:, 0:1]), f64(x.k[:, 0]), f64(x.v[:, 0]), f64(x.dout[:, 0:1]),
+                                       w.P, w.R_lens, w.scale)
+    print(json.dumps({"case": "head_outer", "out": rel(out[:, 0:1], ref["out"].numpy()),
+                      "lse": float(np.abs(lse[0:1].cpu().numpy() - ref["lse"].numpy()).max()),
+                      "dq": rel(g[0][:, 0:1], ref["dq"].numpy()), "dk": rel(g[1][:, 0], ref["dk"].numpy()),
+                      "dv": rel(g[2][:, 0], ref["dv"].numpy()), "status": st, "site": site}), flush=True)
+
 
 if __name__ == "__main__":
     main()

@@ -27,7 +27,7 @@ def test_checks_build_runs_the_parity_cases_clean():
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
-    assert len(lines) == 7, r.stdout
+    assert len(lines) == 8, r.stdout
     for res in lines:
         assert res["status"] == 0 and res["site"] == 0, res
         for key, val in res.items():
