@@ -202,3 +202,24 @@ def test_zero_queries_give_uniform_attention():
     for h in range(w.Hq):
         np.testing.assert_allclose(out[:, h].float().cpu().numpy(), ref, atol=1e-2)
         np.testing.assert_allclose(lse[h].cpu().numpy(), np.log(cnt), atol=1e-4)
+
+
+@pytest.mark.parametrize("d,scale", [(128, 0.3), (64, 0.05)])
+def test_caller_softmax_scale_parity(d, scale):
+    """The softmax scale is the caller's argument: every kernel applies it
+    (scores in the forward and both backward kernels, dK and dQ), not
+    1/sqrt(d).  Every backward mode against the oracle run with that scale."""
+    dk_ = _lib()
+    w = synthetic.make_workload(f"scale_{d}", 4, 2, d, 200, (130, 0, 77))
+    x, (q, k, v, do) = _device_inputs(w, seed=11)
+    f64 = [synthetic.to_f64(t) for t in (x.q, x.k, x.v, x.dout)]
+    ro, rl = ora.dualkv_forward(f64[0], f64[1], f64[2], w.P, w.R_lens, scale)
+    rdq, rdk, rdv = ora.dualkv_backward(*f64, w.P, w.R_lens, scale)
+    out, lse = dk_.forward(q, k, v, w.P, w.R_lens, scale)
+    check_forward(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, w.name)
+    for mode in (0, 1, 2):
+        dq, dkk, dvv = dk_.backward(q, k, v, out, do, lse, w.P, w.R_lens, scale, deterministic=mode)
+        st, site = dk_.dualkv_last_device_error()
+        assert st == 0, (st, site)
+        check_grads({"dq": (dq.float().cpu().numpy(), rdq), "dk": (dkk.float().cpu().numpy(), rdk),
+                     "dv": (dvv.float().cpu().numpy(), rdv)}, f"{w.name} mode={mode}")

@@ -184,6 +184,29 @@ def test_against_torch_sdpa(P, R_lens, Hq, Hkv, d):
         np.testing.assert_allclose(dv, tdv, atol=1e-11)
 
 
+@pytest.mark.parametrize("scale", [0.3, 0.05, 1.7])
+def test_caller_scale_against_torch_sdpa(scale):
+    """The scale is the caller's argument: the oracle with a scale other than
+    1/sqrt(d) matches torch's SDPA given the same scale, and scaling q instead
+    (q -> a*q with the scale divided by a) gives the same out and LSE and a
+    times the dQ."""
+    P, R_lens, Hq, Hkv, d = 37, [5, 0, 19, 1], 4, 2, 8
+    q, k, v, do = rand_case(P, R_lens, Hq, Hkv, d, seed=5)
+    out, lse = ora.dualkv_forward(q, k, v, P, R_lens, scale)
+    dq, dk, dv = ora.dualkv_backward(q, k, v, do, P, R_lens, scale)
+    to, tl, tdq, tdk, tdv = sdpa_packed(q, k, v, do, P, R_lens, scale)
+    for a, b in ((out, to), (lse, tl), (dq, tdq), (dk, tdk), (dv, tdv)):
+        np.testing.assert_allclose(a, b, atol=1e-11)
+    a = 2.5
+    out2, lse2 = ora.dualkv_forward(a * q, k, v, P, R_lens, scale / a)
+    dq2, dk2, dv2 = ora.dualkv_backward(a * q, k, v, do, P, R_lens, scale / a)
+    np.testing.assert_allclose(out2, out, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, atol=1e-12)
+    np.testing.assert_allclose(a * dq2, dq, atol=1e-11)
+    np.testing.assert_allclose(dk2, dk, atol=1e-11)
+    np.testing.assert_allclose(dv2, dv, atol=1e-11)
+
+
 @pytest.mark.slow
 def test_against_torch_sdpa_midsize():
     """One head group of a mid-size case (P=1024, N=4, R=256)."""
