@@ -23,7 +23,7 @@
  *                      sum_j exp(softmax_scale * q . k_j) over the row's visible keys.
  *   R_lens           : HOST array of N int32 response lengths, read during the call.
  *   Grouped-query attention: q-head h reads kv-head h / (Hq / Hkv).
- *   Accepted shapes: d in {64, 128}; Hq % Hkv == 0; 1 <= N <= 1024; P >= 0;
+ *   Accepted shapes: d in {64, 128}; Hq % Hkv == 0; Hq <= 4096; 1 <= N <= 1024; P >= 0;
  *   R_i >= 0; T < 2^31; P and every R_i at most 8388480 rows (65535 tiles of
  *   128); every device pointer 16-byte aligned.  T == 0 is a no-op.  P == 0
  *   gives N independent causal sequences; N == 1 is one causal sequence of
@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
   DUALKV_OK = 0,
   DUALKV_ERR_INVALID_ARG = 1,  /* null pointer, negative length, N out of range, T mismatch */
-  DUALKV_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, a segment over 65535 tiles */
+  DUALKV_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, Hq > 4096, a segment over 65535 tiles */
   DUALKV_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned */
   DUALKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
   DUALKV_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */

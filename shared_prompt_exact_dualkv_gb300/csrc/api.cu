@@ -67,6 +67,8 @@ int check_dims(int32_t Hq, int32_t Hkv, int32_t d) {
   if (Hq < 1 || Hkv < 1) return DUALKV_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DUALKV_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return DUALKV_ERR_UNSUPPORTED;
+  // a launch's grid is (work items) x (heads): at most 4096 x 4096 blocks
+  if (Hq > 4096) return DUALKV_ERR_UNSUPPORTED;
   return DUALKV_OK;
 }
 

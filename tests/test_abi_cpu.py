@@ -76,6 +76,7 @@ def test_fwd_argument_errors(D):
     assert fwd(D, R=_lens(64, -1)) == D.DUALKV_ERR_INVALID_ARG
     assert fwd(D, d=96) == D.DUALKV_ERR_UNSUPPORTED
     assert fwd(D, Hq=3, Hkv=2) == D.DUALKV_ERR_UNSUPPORTED
+    assert fwd(D, Hq=4097, Hkv=1) == D.DUALKV_ERR_UNSUPPORTED   # a grid of items x heads stays in launch limits
     assert fwd(D, Hkv=0) == D.DUALKV_ERR_INVALID_ARG
     assert fwd(D, q=None) == D.DUALKV_ERR_INVALID_ARG
     assert fwd(D, lse=None) == D.DUALKV_ERR_INVALID_ARG
@@ -92,6 +93,7 @@ def test_fwd_argument_errors(D):
 def test_bwd_argument_errors(D):
     assert bwd(D, N=0) == D.DUALKV_ERR_INVALID_ARG
     assert bwd(D, d=32) == D.DUALKV_ERR_UNSUPPORTED
+    assert bwd(D, Hq=8192, Hkv=2) == D.DUALKV_ERR_UNSUPPORTED
     assert bwd(D, dout=None) == D.DUALKV_ERR_INVALID_ARG
     assert bwd(D, dq=A + 4) == D.DUALKV_ERR_ALIGNMENT
     assert bwd(D, ws=None) == D.DUALKV_ERR_WORKSPACE
