@@ -34,8 +34,9 @@
  *   wgu          : [2*inter, hidden] bf16 (gate rows, then up rows)
  *   wd           : [hidden, inter] bf16
  *   gradients    : the same shapes in fp32 (overwritten, not accumulated)
- * Accepted shapes: d in {64, 128}; Hq % Hkv == 0; hidden % 8 == 0 and
- * hidden <= 6144; inter % 8 == 0; the group rules of dualkv_fwd_groups.
+ * Accepted shapes: d in {64, 128}; Hq % Hkv == 0; Hq <= 4096; hidden % 8 == 0
+ * and hidden <= 6144; inter % 8 == 0 and inter <= 2^24; the group rules of
+ * dualkv_fwd_groups.
  *
  * Every step runs in this library's kernels on the caller's stream: the
  * GEMMs on the tcgen05 tensor cores (bf16 inputs, fp32 accumulation, bf16

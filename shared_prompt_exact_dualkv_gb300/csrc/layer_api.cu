@@ -50,7 +50,8 @@ int check_config(const dualkv_layer_config* c) {
   if (c->hidden < 8 || c->Hq < 1 || c->Hkv < 1 || c->inter < 8) return DUALKV_ERR_INVALID_ARG;
   if (!(c->eps >= 0.f) || !std::isfinite(c->eps) || !(c->rope_base > 1.f) || !std::isfinite(c->rope_base))
     return DUALKV_ERR_INVALID_ARG;
-  if (c->hidden % 8 || c->hidden > 6144 || c->inter % 8) return DUALKV_ERR_UNSUPPORTED;
+  if (c->hidden % 8 || c->hidden > 6144 || c->inter % 8 || c->inter > (1 << 24) || c->Hq > 4096)
+    return DUALKV_ERR_UNSUPPORTED;
   if ((c->d != 64 && c->d != 128) || c->Hq % c->Hkv) return DUALKV_ERR_UNSUPPORTED;
   return DUALKV_OK;
 }

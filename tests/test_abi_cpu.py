@@ -203,7 +203,8 @@ def test_layer_argument_errors(D):
     assert D.dualkv_layer_workspace_bytes(cfg, groups) > 0
     for bad, code in ((D.layer_config(256, 4, 2, 96, 512), 0), (D.layer_config(252, 4, 2, 64, 512), 0),
                       (D.layer_config(256, 3, 2, 64, 512), 0), (D.layer_config(256, 4, 2, 64, 512, eps=-1.0), 0),
-                      (D.layer_config(256, 4, 2, 64, 512, rope_base=0.5), 0)):
+                      (D.layer_config(256, 4, 2, 64, 512, rope_base=0.5), 0),
+                      (D.layer_config(256, 8192, 2, 64, 512), 0), (D.layer_config(256, 4, 2, 64, (1 << 24) + 8), 0)):
         assert D.dualkv_layer_workspace_bytes(bad, groups) == code
     assert D.dualkv_layer_workspace_bytes(cfg, [(-1, (4,))]) == 0
     G, Ps, Ns, Rs = D._groups(groups)
