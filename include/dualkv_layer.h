@@ -134,8 +134,9 @@ DUALKV_API int dualkv_packed_positions(int32_t G, const int64_t* P, const int32_
  *   kind 2: Y[M,N] = A[K,M]^T . B[K,N], fp32 Y (zeros when K == 0).
  * Every row length of A, B and Y (the contiguous dimension) must be a
  * multiple of 8, and every pointer 16-byte aligned.  M, N, K >= 0 and below
- * 2^31.  Returns DUALKV_OK, DUALKV_ERR_INVALID_ARG, DUALKV_ERR_UNSUPPORTED
- * (a row length not a multiple of 8), DUALKV_ERR_ALIGNMENT or DUALKV_ERR_CUDA.
+ * 2^31, M * N at most 2^40.  Returns DUALKV_OK, DUALKV_ERR_INVALID_ARG,
+ * DUALKV_ERR_UNSUPPORTED (a row length not a multiple of 8, or M * N over
+ * 2^40), DUALKV_ERR_ALIGNMENT or DUALKV_ERR_CUDA.
  */
 DUALKV_API int dualkv_gemm(int32_t kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* Y,
                            int32_t accumulate, void* stream);

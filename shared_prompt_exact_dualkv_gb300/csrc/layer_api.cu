@@ -323,6 +323,8 @@ int dualkv_gemm(int32_t kind, int64_t M, int64_t N, int64_t K, const void* A, co
   if (kind < 0 || kind > 2 || M < 0 || N < 0 || K < 0) return DUALKV_ERR_INVALID_ARG;
   const int64_t lim = (int64_t(1) << 31) - 1;
   if (M > lim || N > lim || K > lim) return DUALKV_ERR_INVALID_ARG;
+  // tile counts are int: at most 2^40 output elements
+  if (M * N > (int64_t(1) << 40)) return DUALKV_ERR_UNSUPPORTED;
   // row lengths of A, B and Y
   const int64_t la = kind == 2 ? M : K, lb = kind == 0 ? K : N;
   if (la % 8 || lb % 8 || N % 8) return DUALKV_ERR_UNSUPPORTED;

@@ -295,3 +295,16 @@ def test_checks_build_compiles_and_reports_itself(D):
                        capture_output=True, text=True, timeout=300)
     assert r.stdout.split() == ["1", "True"], r.stdout + r.stderr
     assert D.lib.dualkv_checks_enabled() == 0
+
+
+def test_gemm_argument_errors(D):
+    """dualkv_gemm rejects bad arguments before anything touches the GPU."""
+    g = lambda kind=0, M=64, N=64, K=64, a=A, b=A, y=A: D.lib.dualkv_gemm(kind, M, N, K, a, b, y, 0, None)
+    assert g(kind=3) == D.DUALKV_ERR_INVALID_ARG
+    assert g(M=-1) == D.DUALKV_ERR_INVALID_ARG
+    assert g(K=1 << 31) == D.DUALKV_ERR_INVALID_ARG
+    assert g(N=12) == D.DUALKV_ERR_UNSUPPORTED                  # a row length not a multiple of 8
+    assert g(M=(1 << 31) - 8, N=(1 << 20)) == D.DUALKV_ERR_UNSUPPORTED   # M * N over 2^40
+    assert g(y=None) == D.DUALKV_ERR_INVALID_ARG
+    assert g(a=A + 8) == D.DUALKV_ERR_ALIGNMENT
+    assert g(M=0) == D.DUALKV_OK                                # empty output: nothing to do
