@@ -562,7 +562,7 @@ const char* dualkv_status_string(int status) {
   switch (status) {
     case DUALKV_OK: return "ok";
     case DUALKV_ERR_INVALID_ARG: return "invalid argument";
-    case DUALKV_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, Hq % Hkv == 0, each prompt or response at most 8388480 rows)";
+    case DUALKV_ERR_UNSUPPORTED: return "unsupported shape (outside the accepted shapes the entry point documents)";
     case DUALKV_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
     case DUALKV_ERR_WORKSPACE: return "workspace missing or too small";
     case DUALKV_ERR_CUDA: return "CUDA runtime or launch error";

@@ -102,6 +102,23 @@ def main():
                       "dq": rel(g[0][:, 0:1], ref["dq"].numpy()), "dk": rel(g[1][:, 0], ref["dk"].numpy()),
                       "dv": rel(g[2][:, 0], ref["dv"].numpy()), "status": st, "site": site}), flush=True)
 
+    # the layer's GEMM in all three forms, on the 128-row tile path and the
+    # 256-row one (19000 x 2056 has 675 tiles of 256 x 256), against fp64 products
+    g = torch.Generator("cpu").manual_seed(8)
+    worst = 0.0
+    for M, N, K in ((296, 264, 200), (19000, 2056, 200)):   # every row length a multiple of 8
+        for kind in (0, 1, 2):
+            shapes = {0: ((M, K), (N, K)), 1: ((M, K), (K, N)), 2: ((K, M), (K, N))}[kind]
+            A = torch.randn(shapes[0], generator=g).to(torch.bfloat16)
+            B = torch.randn(shapes[1], generator=g).to(torch.bfloat16)
+            ref = {0: lambda: A.double() @ B.double().T, 1: lambda: A.double() @ B.double(),
+                   2: lambda: A.double().T @ B.double()}[kind]()
+            Y = torch.full((M, N), float("nan"), dtype=torch.float32 if kind == 2 else torch.bfloat16, device="cuda")
+            D.dualkv_gemm(kind, A.cuda(), B.cuda(), Y)
+            worst = max(worst, rel(Y, ref.numpy()))
+    st, site = D.dualkv_last_device_error()
+    print(json.dumps({"case": "gemm", "gemm": worst, "status": st, "site": site}), flush=True)
+
 
 if __name__ == "__main__":
     main()
