@@ -509,15 +509,40 @@ def _oracle_seq0_inputs(w: synthetic.Workload, seed: int):
 
 def oracle_sample_seconds(w: synthetic.Workload, seed: int = 0):
     """The fp64 oracle (as it stands) on one q-head and sequence 0 of the
-    workload: replicated fwd + bwd of [prompt ; response_0]."""
+    workload: replicated fwd + bwd of [prompt ; response_0].  Returns the
+    seconds, the useful flops and (inputs, outputs) for sample_parity."""
     from oracle import attention as ora
     q, k, v, do = _oracle_seq0_inputs(w, seed)
     t0 = time.perf_counter()
-    ora.dualkv_forward(q, k, v, w.P, (w.R_lens[0],), w.scale)
-    ora.dualkv_backward(q, k, v, do, w.P, (w.R_lens[0],), w.scale)
+    out, lse = ora.dualkv_forward(q, k, v, w.P, (w.R_lens[0],), w.scale)
+    dq, dk, dv = ora.dualkv_backward(q, k, v, do, w.P, (w.R_lens[0],), w.scale)
     dt = time.perf_counter() - t0
     sub = synthetic.make_workload("s", 1, 1, w.d, w.P, (w.R_lens[0],))
-    return dt, sub.useful_flops()
+    return dt, sub.useful_flops(), (q, k, v, do, out, lse, dq, dk, dv)
+
+
+def sample_parity(D, w: synthetic.Workload, dev, stream, sample):
+    """The library on the oracle sample's own inputs (one head, [prompt ;
+    response_0] at the workload's P, R_0, d and scale), compared element by
+    element with the oracle's outputs, outside the timed region."""
+    q, k, v, do, ro, rl, rdq, rdk, rdv = sample
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(dev)   # exact: the inputs are bf16 values
+    tq, tk, tv, tdo = (bf(a) for a in (q, k, v, do))
+    R = (w.R_lens[0],)
+    with torch.cuda.stream(stream):
+        out, lse = D.forward(tq, tk, tv, w.P, R, w.scale, stream=stream)
+        dq, dk, dv = D.backward(tq, tk, tv, out, tdo, lse, w.P, R, w.scale, stream=stream)
+    torch.cuda.synchronize()
+    f = lambda t: t.float().cpu().double().numpy()
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+    res = {"rows": int(q.shape[0]), "heads": 1,
+           "out_max_abs": float(np.abs(f(out) - ro).max()), "out_rel_l2": rel(f(out), ro),
+           "lse_max_abs": float(np.abs(f(lse) - rl).max()),
+           "dq_rel_l2": rel(f(dq), rdq), "dk_rel_l2": rel(f(dk), rdk), "dv_rel_l2": rel(f(dv), rdv)}
+    res["within_bounds"] = bool(res["out_max_abs"] <= 1e-2 and res["out_rel_l2"] <= 5e-3 and
+                                res["lse_max_abs"] <= 1e-3 and
+                                max(res["dq_rel_l2"], res["dk_rel_l2"], res["dv_rel_l2"]) <= 1e-2)
+    return res
 
 
 def oracle_rows_seconds(w: synthetic.Workload, rows: int, seed: int = 0):
@@ -804,7 +829,9 @@ def main():
         del rq, rk, rv, rdo, rout, rlse, rdq, rdk, rdv, rws
         torch.cuda.empty_cache()
         if world == 1:
-            dt, fl = oracle_sample_seconds(w)
+            dt, fl, sample = oracle_sample_seconds(w)
+            result["parity_sample"] = sample_parity(D, w, dev, stream, sample)
+            del sample
             # The replicated oracle's cost is linear in heads and, per sequence,
             # in its causal pairs: scale the one (head, sequence) sample to the
             # whole step.
